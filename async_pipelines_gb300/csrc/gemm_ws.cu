@@ -1,0 +1,290 @@
+// Host side of the C ABI declared in include/gemm_ws.h: argument checks (the
+// `can_implement` role of "sm90_gemm_tma_warpspecialized_cooperative.hpp"),
+// TMA descriptor encoding, the tiny device workspace, and the launch of the
+// persistent kernel (grid = min(#SMs, #tiles), one CTA per SM).
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+
+#include "gemm_ws.h"
+#include "gemm_ws_kernel.cuh"
+
+struct gemm_ws {
+  int device;
+  int num_sms;
+  uint32_t* work;                 // [0] stream-out counter, [1] status word
+  int last_cuda_error;
+  unsigned long long timeout_ns;
+  PFN_cuTensorMapEncodeTiled_v12000 encode;
+};
+
+namespace {
+
+constexpr int64_t kMaxDim = (int64_t{1} << 31) - 1;
+constexpr int64_t kMaxElems = int64_t{1} << 40;
+
+int cuda_fail(gemm_ws* h, cudaError_t e) {
+  if (h) h->last_cuda_error = static_cast<int>(e);
+  return GEMM_WS_ERR_CUDA;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool overlaps(const void* a, int64_t abytes, const void* b, int64_t bbytes) {
+  if (!a || !b || abytes <= 0 || bbytes <= 0) return false;
+  const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+  return a0 < b0 + static_cast<uintptr_t>(bbytes) && b0 < a0 + static_cast<uintptr_t>(abytes);
+}
+
+// A 3-D bf16 tensor {d0 (contiguous), d1, d2}, packed, tiled box {b0, b1, 1}.
+CUresult encode3d(gemm_ws* h, CUtensorMap* m, const void* ptr, uint64_t d0, uint64_t d1,
+                  uint64_t d2, uint32_t b0, uint32_t b1, CUtensorMapSwizzle sw,
+                  CUtensorMapL2promotion promo) {
+  cuuint64_t dims[3] = {d0, d1, d2};
+  cuuint64_t strides[2] = {d0 * 2, d0 * d1 * 2};
+  cuuint32_t box[3] = {b0, b1, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return h->encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw, promo,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
+int check_problem(gemm_ws* h, const uint16_t* A, const uint16_t* B, const uint16_t* C,
+                  uint16_t* D, int64_t M, int64_t N, int64_t K, int64_t L, float beta) {
+  if (!h) return GEMM_WS_ERR_INVALID_ARG;
+  if (M < 0 || N < 0 || K < 0 || L < 0) return GEMM_WS_ERR_INVALID_ARG;
+  if (M > kMaxDim || N > kMaxDim || K > kMaxDim || L > kMaxDim) return GEMM_WS_ERR_INVALID_ARG;
+  if (M * N * L == 0) return GEMM_WS_OK;   // nothing to do; pointers unchecked
+  if (L * M > kMaxElems / (N > 0 ? N : 1) || L * M > kMaxElems / (K > 0 ? K : 1) ||
+      L * N > kMaxElems / (K > 0 ? K : 1))
+    return GEMM_WS_ERR_INVALID_ARG;
+  if (!D) return GEMM_WS_ERR_INVALID_ARG;
+  if (K > 0 && (!A || !B)) return GEMM_WS_ERR_INVALID_ARG;
+  if (beta != 0.0f && !C) return GEMM_WS_ERR_INVALID_ARG;
+  if ((K % 8) != 0 || (N % 8) != 0) return GEMM_WS_ERR_ALIGNMENT;
+  if (!aligned16(D) || (K > 0 && (!aligned16(A) || !aligned16(B))) ||
+      (beta != 0.0f && !aligned16(C)))
+    return GEMM_WS_ERR_ALIGNMENT;
+  const int64_t dbytes = 2 * L * M * N;
+  if (K > 0 && (overlaps(D, dbytes, A, 2 * L * M * K) || overlaps(D, dbytes, B, 2 * L * N * K)))
+    return GEMM_WS_ERR_INVALID_ARG;
+  if (beta != 0.0f && C != D && overlaps(D, dbytes, C, dbytes)) return GEMM_WS_ERR_INVALID_ARG;
+  return GEMM_WS_OK;
+}
+
+int launch(gemm_ws* h, const uint16_t* A, const uint16_t* B, const uint16_t* C, uint16_t* D,
+           int64_t M, int64_t N, int64_t K, int64_t L, float alpha, float beta,
+           uint16_t* staging, uint32_t* flags, cudaStream_t stream) {
+  gws::Params p;
+  std::memset(&p, 0, sizeof p);
+  const int64_t tiles_m = (M + gws::BM - 1) / gws::BM;
+  const int64_t tiles_n = (N + gws::BN - 1) / gws::BN;
+  const int64_t num_tiles = L * tiles_m * tiles_n;
+  if (num_tiles > kMaxDim) return GEMM_WS_ERR_INVALID_ARG;
+  const int64_t stn = (N + gws::STAGING - 1) / gws::STAGING;
+  const int64_t T = L * tiles_m * stn;
+
+  CUresult r = CUDA_SUCCESS;
+  if (K > 0) {
+    r = encode3d(h, &p.tmA, A, K, M, L, gws::BK, gws::BM, CU_TENSOR_MAP_SWIZZLE_128B,
+                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+    if (r == CUDA_SUCCESS)
+      r = encode3d(h, &p.tmB, B, K, N, L, gws::BK, gws::BN, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+  }
+  if (r == CUDA_SUCCESS && beta != 0.0f)
+    r = encode3d(h, &p.tmC, C, N, M, L, gws::EPI_N, 32, CU_TENSOR_MAP_SWIZZLE_64B,
+                 CU_TENSOR_MAP_L2_PROMOTION_NONE);
+  if (r == CUDA_SUCCESS)
+    r = encode3d(h, &p.tmD, D, N, M, L, gws::EPI_N, 32, CU_TENSOR_MAP_SWIZZLE_64B,
+                 CU_TENSOR_MAP_L2_PROMOTION_NONE);
+  if (r == CUDA_SUCCESS && staging)
+    r = encode3d(h, &p.tmS, staging, gws::STAGING, gws::STAGING, static_cast<uint64_t>(T),
+                 gws::EPI_N, gws::STAGING, CU_TENSOR_MAP_SWIZZLE_64B,
+                 CU_TENSOR_MAP_L2_PROMOTION_NONE);
+  if (r != CUDA_SUCCESS) {
+    h->last_cuda_error = static_cast<int>(r);
+    return GEMM_WS_ERR_CUDA;
+  }
+
+  p.M = static_cast<int>(M);
+  p.N = static_cast<int>(N);
+  p.K = static_cast<int>(K);
+  p.L = static_cast<int>(L);
+  p.tiles_m = static_cast<int>(tiles_m);
+  p.tiles_n = static_cast<int>(tiles_n);
+  p.num_tiles = static_cast<int>(num_tiles);
+  p.num_kb = static_cast<int>((K + gws::BK - 1) / gws::BK);
+  p.group_m = 16;
+  p.staging_tiles_n = static_cast<int>(stn);
+  p.alpha = alpha;
+  p.beta = beta;
+  p.has_c = beta != 0.0f ? 1 : 0;
+  p.streamout = staging ? 1 : 0;
+  p.flags = flags;
+  p.counter = h->work;
+  p.status = h->work + 1;
+  p.timeout_ns = h->timeout_ns;
+
+  cudaError_t e;
+  if (staging) {
+    e = cudaMemsetAsync(flags, 0, static_cast<size_t>(2 * T) * sizeof(uint32_t), stream);
+    if (e == cudaSuccess) e = cudaMemsetAsync(h->work, 0, sizeof(uint32_t), stream);
+    if (e != cudaSuccess) return cuda_fail(h, e);
+  }
+  const int grid = static_cast<int>(num_tiles < h->num_sms ? num_tiles : h->num_sms);
+  gws::gemm_ws_kernel<<<grid, gws::NUM_THREADS, gws::SMEM_BYTES, stream>>>(p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(h, e);
+  return GEMM_WS_OK;
+}
+
+class DeviceGuard {
+ public:
+  explicit DeviceGuard(int dev) {
+    if (cudaGetDevice(&prev_) != cudaSuccess) prev_ = -1;
+    if (prev_ != dev) cudaSetDevice(dev);
+  }
+  ~DeviceGuard() {
+    int cur = -1;
+    if (prev_ >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev_) cudaSetDevice(prev_);
+  }
+
+ private:
+  int prev_ = -1;
+};
+
+}  // namespace
+
+extern "C" {
+
+int gemm_ws_create(gemm_ws_t** out, int device) {
+  if (!out) return GEMM_WS_ERR_INVALID_ARG;
+  *out = nullptr;
+  int count = 0;
+  cudaError_t e = cudaGetDeviceCount(&count);
+  if (e != cudaSuccess) return GEMM_WS_ERR_CUDA;
+  if (device < 0 || device >= count) return GEMM_WS_ERR_INVALID_ARG;
+  DeviceGuard guard(device);
+  cudaDeviceProp prop;
+  e = cudaGetDeviceProperties(&prop, device);
+  if (e != cudaSuccess) return GEMM_WS_ERR_CUDA;
+  if (prop.major != 10 || prop.minor != 3) return GEMM_WS_ERR_UNSUPPORTED;
+
+  gemm_ws* h = static_cast<gemm_ws*>(std::calloc(1, sizeof(gemm_ws)));
+  if (!h) return GEMM_WS_ERR_CUDA;
+  h->device = device;
+  h->num_sms = prop.multiProcessorCount;
+  h->timeout_ns = 1000000000ull;   // 1 s per wait
+  if (const char* s = std::getenv("GEMM_WS_TIMEOUT_MS")) {
+    const long long ms = std::atoll(s);
+    if (ms > 0) h->timeout_ns = static_cast<unsigned long long>(ms) * 1000000ull;
+  }
+
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                       &q);
+  if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn) {
+    std::free(h);
+    return GEMM_WS_ERR_CUDA;
+  }
+  h->encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+
+  e = cudaFuncSetAttribute(gws::gemm_ws_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(gws::SMEM_BYTES));
+  if (e == cudaSuccess) e = cudaMalloc(&h->work, 2 * sizeof(uint32_t));
+  if (e == cudaSuccess) e = cudaMemset(h->work, 0, 2 * sizeof(uint32_t));
+  if (e != cudaSuccess) {
+    if (h->work) cudaFree(h->work);
+    std::free(h);
+    return GEMM_WS_ERR_CUDA;
+  }
+  *out = h;
+  return GEMM_WS_OK;
+}
+
+int gemm_ws_destroy(gemm_ws_t* h) {
+  if (!h) return GEMM_WS_OK;
+  DeviceGuard guard(h->device);
+  cudaDeviceSynchronize();
+  cudaFree(h->work);
+  std::free(h);
+  return GEMM_WS_OK;
+}
+
+int gemm_ws_run(gemm_ws_t* h, const uint16_t* A, const uint16_t* B, const uint16_t* C,
+                uint16_t* D, int64_t M, int64_t N, int64_t K, int64_t L, float alpha,
+                float beta, void* stream) {
+  int rc = check_problem(h, A, B, C, D, M, N, K, L, beta);
+  if (rc != GEMM_WS_OK || M * N * L == 0) return rc;
+  DeviceGuard guard(h->device);
+  return launch(h, A, B, C, D, M, N, K, L, alpha, beta, nullptr, nullptr,
+                static_cast<cudaStream_t>(stream));
+}
+
+int gemm_ws_run_streamout(gemm_ws_t* h, const uint16_t* A, const uint16_t* B,
+                          const uint16_t* C, uint16_t* D, int64_t M, int64_t N, int64_t K,
+                          int64_t L, float alpha, float beta, uint16_t* staging,
+                          uint32_t* flags, void* stream) {
+  int rc = check_problem(h, A, B, C, D, M, N, K, L, beta);
+  if (rc != GEMM_WS_OK || M * N * L == 0) return rc;
+  if (!staging || !flags) return GEMM_WS_ERR_INVALID_ARG;
+  if (!aligned16(staging) || (reinterpret_cast<uintptr_t>(flags) & 7u) != 0)
+    return GEMM_WS_ERR_ALIGNMENT;
+  const int64_t T = gemm_ws_streamout_tiles(M, N, L);
+  const int64_t sbytes = T * gws::STAGING * gws::STAGING * 2, fbytes = 2 * T * 4;
+  const int64_t dbytes = 2 * L * M * N;
+  if (overlaps(staging, sbytes, flags, fbytes) || overlaps(staging, sbytes, D, dbytes) ||
+      overlaps(flags, fbytes, D, dbytes) ||
+      (K > 0 && (overlaps(staging, sbytes, A, 2 * L * M * K) ||
+                 overlaps(staging, sbytes, B, 2 * L * N * K) ||
+                 overlaps(flags, fbytes, A, 2 * L * M * K) ||
+                 overlaps(flags, fbytes, B, 2 * L * N * K))) ||
+      (beta != 0.0f && (overlaps(staging, sbytes, C, dbytes) || overlaps(flags, fbytes, C, dbytes))))
+    return GEMM_WS_ERR_INVALID_ARG;
+  DeviceGuard guard(h->device);
+  return launch(h, A, B, C, D, M, N, K, L, alpha, beta, staging, flags,
+                static_cast<cudaStream_t>(stream));
+}
+
+int gemm_ws_query_status(gemm_ws_t* h, void* stream) {
+  if (!h) return GEMM_WS_ERR_INVALID_ARG;
+  DeviceGuard guard(h->device);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(h, e);
+  uint32_t st = 0;
+  e = cudaMemcpy(&st, h->work + 1, sizeof st, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(h, e);
+  if (st != 0) {
+    e = cudaMemset(h->work + 1, 0, sizeof(uint32_t));
+    if (e != cudaSuccess) return cuda_fail(h, e);
+  }
+  return static_cast<int>(st);
+}
+
+int gemm_ws_last_cuda_error(gemm_ws_t* h) { return h ? h->last_cuda_error : 0; }
+
+const char* gemm_ws_status_string(int status) {
+  switch (status) {
+    case GEMM_WS_OK: return "ok";
+    case GEMM_WS_ERR_INVALID_ARG: return "invalid argument";
+    case GEMM_WS_ERR_ALIGNMENT: return "misaligned pointer or row pitch";
+    case GEMM_WS_ERR_UNSUPPORTED: return "unsupported device (needs sm_103)";
+    case GEMM_WS_ERR_CUDA: return "CUDA error";
+    case GEMM_WS_ERR_TIMEOUT: return "device wait timed out";
+    default: return "unknown status";
+  }
+}
+
+int64_t gemm_ws_streamout_tiles(int64_t M, int64_t N, int64_t L) {
+  if (M <= 0 || N <= 0 || L <= 0) return 0;
+  return L * ((M + gws::STAGING - 1) / gws::STAGING) * ((N + gws::STAGING - 1) / gws::STAGING);
+}
+
+}  // extern "C"

@@ -1,0 +1,505 @@
+// Persistent warp-specialized bf16 GEMM for GB300 (sm_103a), one CTA per SM.
+//
+//   D[l] = alpha * A[l] * B[l] + beta * C[l]     (fp32 accumulate in TMEM)
+//
+// Warp roles (the SM90 cooperative kernel's producer / consumer / epilogue
+// split of "sm90_gemm_tma_warpspecialized_cooperative.hpp", re-cut for
+// tcgen05, whose accumulators live in tensor memory instead of registers):
+//   warp 0     TMA producer: fills a STAGES-deep shared-memory ring of A/B
+//              k-blocks guarded by full/empty mbarriers. Like the SM100
+//              mainloop `load()` discussed in "why does load() pre-issue
+//              producer_try_acquire", it probes the NEXT stage's empty barrier
+//              (non-blocking token) before issuing the current stage's copies.
+//   warp 1     MMA issuer: one thread issues tcgen05.mma (128 x 256 x 16)
+//              into one of two TMEM accumulators and releases each stage with
+//              tcgen05.commit -> empty[s]; a tile's last commit -> acc_full.
+//   warps 2-5  epilogue: each warp owns one 32-lane quarter of TMEM (rows),
+//              drains 32-column subtiles TMEM -> registers, applies
+//              alpha/beta (C arrives by TMA), rounds to bf16, writes a
+//              swizzled shared-memory slot and TMA-stores it to D over a
+//              two-slot store pipeline (bulk-group read waits), as in the
+//              Hopper epilogue loop quoted in "How to build a pipeline between
+//              epilogue and communication warp groups?".
+//   warp 6     stream-out consumer (optional): the per-tile handoff that issue
+//              asks for. The epilogue arrives on d_full[slot] after writing a
+//              slot; the consumer waits on it, copies the slot into a packed
+//              staging buffer with its own TMA store, waits for that store's
+//              shared-memory reads, and arrives on d_empty[slot]. The epilogue
+//              reuses a slot only after BOTH its own bulk-group read wait and
+//              d_empty, which is the answer to the issue's problem that bulk
+//              groups are per thread and invisible to another warp.
+//
+// Every role walks the same static persistent tile sequence (tile
+// blockIdx.x, then + gridDim.x, ...), so the scheduler needs no communication.
+// Every wait is bounded by a watchdog (global timer): on expiry the kernel
+// records GEMM_WS_ERR_TIMEOUT in a status word, all roles leave their loops,
+// in-flight copies are drained and TMEM is freed.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "ptx.cuh"
+
+namespace gws {
+
+constexpr int BM = 128;                  // tile rows   (UMMA M)
+constexpr int BN = 256;                  // tile cols   (UMMA N)
+constexpr int BK = 64;                   // k-block: 64 bf16 = one 128-byte swizzle row
+constexpr int UMMA_K = 16;               // K of one tcgen05.mma kind::f16
+constexpr int STAGES = 4;                // mainloop ring depth
+constexpr int ACC_BUFS = 2;              // TMEM accumulators (MMA overlaps epilogue)
+constexpr int EPI_N = 32;                // columns per epilogue subtile
+constexpr int EPI_SUB = BN / EPI_N;      // subtiles per tile
+constexpr int EPI_SLOTS = 2;             // D shared-memory slots (store pipeline depth)
+constexpr int C_BUFS = 2;                // C shared-memory buffers per epilogue warp
+constexpr int NUM_EPI_WARPS = 4;
+constexpr int STAGING = 128;             // stream-out tile edge
+constexpr int SUB_PER_STAGING = STAGING / EPI_N;
+constexpr int WARP_TMA = 0;
+constexpr int WARP_MMA = 1;
+constexpr int WARP_EPI0 = 2;
+constexpr int WARP_CONSUMER = 6;
+constexpr int NUM_THREADS = 7 * 32;
+constexpr uint32_t TMEM_COLS = ACC_BUFS * BN;   // 512: all of the SM's TMEM
+
+constexpr uint32_t A_STAGE_BYTES = BM * BK * 2;          // 16 KiB
+constexpr uint32_t B_STAGE_BYTES = BN * BK * 2;          // 32 KiB
+constexpr uint32_t STAGE_TX_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
+constexpr uint32_t EPI_QUARTER_BYTES = 32 * EPI_N * 2;   // 2 KiB: one warp's rows
+constexpr uint32_t EPI_SLOT_BYTES = BM * EPI_N * 2;      // 8 KiB: 128 rows
+
+// Shared-memory carve-out (offsets from a 1024-byte aligned base).
+constexpr uint32_t OFF_A = 0;
+constexpr uint32_t OFF_B = OFF_A + STAGES * A_STAGE_BYTES;
+constexpr uint32_t OFF_D = OFF_B + STAGES * B_STAGE_BYTES;
+constexpr uint32_t OFF_C = OFF_D + EPI_SLOTS * EPI_SLOT_BYTES;
+constexpr uint32_t OFF_BAR = OFF_C + C_BUFS * EPI_SLOT_BYTES;
+// barrier indices
+constexpr int BAR_FULL = 0;
+constexpr int BAR_EMPTY = BAR_FULL + STAGES;
+constexpr int BAR_ACC_FULL = BAR_EMPTY + STAGES;
+constexpr int BAR_ACC_EMPTY = BAR_ACC_FULL + ACC_BUFS;
+constexpr int BAR_C_FULL = BAR_ACC_EMPTY + ACC_BUFS;          // [warp quarter][buf]
+constexpr int BAR_D_FULL = BAR_C_FULL + NUM_EPI_WARPS * C_BUFS;
+constexpr int BAR_D_EMPTY = BAR_D_FULL + EPI_SLOTS;
+constexpr int BAR_MMA_DRAIN = BAR_D_EMPTY + EPI_SLOTS;
+constexpr int NUM_BARS = BAR_MMA_DRAIN + 1;
+constexpr uint32_t OFF_TMEM_SLOT = OFF_BAR + NUM_BARS * 8;
+constexpr uint32_t OFF_ABORT = OFF_TMEM_SLOT + 4;
+constexpr uint32_t SMEM_USED = OFF_ABORT + 4;
+constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;   // + slack to align the base
+static_assert(SMEM_BYTES <= 232448, "exceeds the 227 KiB per-CTA shared memory");
+static_assert(OFF_B % 1024 == 0 && OFF_D % 1024 == 0 && OFF_C % 1024 == 0, "alignment");
+
+constexpr uint32_t STATUS_TIMEOUT = 5;   // == GEMM_WS_ERR_TIMEOUT
+
+struct Params {
+  CUtensorMap tmA;   // {K, M, L}, box {64, 128}, 128-byte swizzle
+  CUtensorMap tmB;   // {K, N, L}, box {64, 256}, 128-byte swizzle
+  CUtensorMap tmC;   // {N, M, L}, box {32, 32},  64-byte swizzle (beta != 0)
+  CUtensorMap tmD;   // {N, M, L}, box {32, 32},  64-byte swizzle
+  CUtensorMap tmS;   // staging {128, 128, T}, box {32, 128}, 64-byte swizzle
+  int M, N, K, L;
+  int tiles_m, tiles_n, num_tiles, num_kb;
+  int group_m;                   // raster: tiles walk group_m m-tiles per n step
+  int staging_tiles_n;           // ceil(N / 128)
+  float alpha, beta;
+  int has_c;                     // beta != 0
+  int streamout;
+  uint32_t* flags;               // 2 * T words (stream-out)
+  uint32_t* counter;             // stream-out sequence counter (zeroed by host)
+  uint32_t* status;              // watchdog status word
+  unsigned long long timeout_ns; // bound of every single wait
+};
+
+// Tile t -> (m block, n block, batch). Within a batch, tiles go down a group
+// of `group_m` m-blocks, then step n, so the CTAs resident at one time share
+// their A rows and B columns through L2.
+__device__ __forceinline__ void tile_coords(const Params& p, int t, int& mb, int& nb, int& l) {
+  const int per_batch = p.tiles_m * p.tiles_n;
+  l = t / per_batch;
+  const int r = t - l * per_batch;
+  const int group_tiles = p.group_m * p.tiles_n;
+  const int g = r / group_tiles;
+  const int first_m = g * p.group_m;
+  const int gm = min(p.tiles_m - first_m, p.group_m);
+  const int rr = r - g * group_tiles;
+  mb = first_m + rr % gm;
+  nb = rr / gm;
+}
+
+// Stream-out tiles (128 columns) of output tile `nb` that exist: 1 or 2.
+__device__ __forceinline__ int staging_in_tile(const Params& p, int nb) {
+  const int cols_left = p.N - nb * BN;
+  return min(BN / STAGING, (cols_left + STAGING - 1) / STAGING);
+}
+
+struct Watchdog {
+  volatile uint32_t* abort;   // shared-memory abort flag of this CTA
+  uint32_t* status;           // global status word
+  unsigned long long limit_ns;
+};
+
+// Bounded wait on an mbarrier phase. Returns false if the CTA is aborting or
+// this wait exceeded the limit (which then starts the abort).
+__device__ __noinline__ bool wait_bounded(uint32_t bar, uint32_t parity, const Watchdog& wd) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 7) == 0) {
+      if (*wd.abort) return false;
+      if (global_timer_ns() - t0 > wd.limit_ns) {
+        *wd.abort = 1;
+        atomicExch(wd.status, STATUS_TIMEOUT);
+        return false;
+      }
+    }
+  }
+}
+
+// Short bounded wait used only while draining after an abort.
+__device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity) {
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (global_timer_ns() - t0 > 100000000ull) return;   // 100 ms
+  }
+}
+
+// Warp-uniform wait: lane 0 waits, the verdict is broadcast to the warp.
+// On success every lane then probes the (already completed) phase once, so
+// each thread itself observes the completion (acquire) before touching the
+// data it guards. The phase cannot move on meanwhile: its next completion
+// needs an arrival that this warp makes only later.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const Watchdog& wd) {
+  uint32_t ok = 0;
+  if ((threadIdx.x & 31) == 0) ok = wait_bounded(bar, parity, wd) ? 1u : 0u;
+  ok = __shfl_sync(0xffffffffu, ok, 0);
+  if (ok) (void)mbar_try_wait(bar, parity);
+  __syncwarp();
+  return ok != 0;
+}
+
+// ------------------------------------------------------------ producer
+
+__device__ __forceinline__ void producer_role(const Params& p, uint32_t sbase,
+                                              const Watchdog& wd) {
+  auto full = [&](uint32_t s) { return sbase + OFF_BAR + 8 * (BAR_FULL + s); };
+  auto empty = [&](uint32_t s) { return sbase + OFF_BAR + 8 * (BAR_EMPTY + s); };
+  uint32_t g = 0;   // k-blocks issued by this CTA so far (ring position)
+  bool ok = true;
+  // The producer starts in the opposite phase: the first STAGES waits on a
+  // freshly initialised empty barrier (parity 1) succeed at once.
+  bool token = mbar_test_wait(empty(0), 1);
+  for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+    int mb, nb, l;
+    tile_coords(p, t, mb, nb, l);
+    const int m0 = mb * BM, n0 = nb * BN;
+    for (int kb = 0; kb < p.num_kb; ++kb) {
+      const uint32_t s = g % STAGES;
+      const uint32_t ph = (g / STAGES) & 1;
+      if (!token && !wait_bounded(empty(s), ph ^ 1, wd)) {
+        ok = false;
+        break;
+      }
+      ++g;
+      // try-acquire the NEXT stage before this stage's copies go out
+      token = mbar_test_wait(empty(g % STAGES), ((g / STAGES) & 1) ^ 1);
+      mbar_arrive_expect_tx(full(s), STAGE_TX_BYTES);
+      tma_load_3d(sbase + OFF_A + s * A_STAGE_BYTES, &p.tmA, full(s), kb * BK, m0, l);
+      tma_load_3d(sbase + OFF_B + s * B_STAGE_BYTES, &p.tmB, full(s), kb * BK, n0, l);
+    }
+  }
+  if (!ok) {
+    // Abort: wait (bounded) for the copies of the last stages issued, so no
+    // TMA write lands after the CTA has released its shared memory.
+    const uint32_t first = g > STAGES ? g - STAGES : 0;
+    for (uint32_t j = first; j < g; ++j) wait_drain(full(j % STAGES), (j / STAGES) & 1);
+  }
+}
+
+// ------------------------------------------------------------ MMA issuer
+
+__device__ __forceinline__ void mma_role(const Params& p, uint32_t sbase, uint32_t tmem_base,
+                                         const Watchdog& wd) {
+  auto bar = [&](int i) { return sbase + OFF_BAR + 8 * i; };
+  constexpr uint32_t idesc = idesc_bf16_f32(BM, BN);
+  uint32_t g = 0;
+  int i = 0;
+  bool issued = false;
+  for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++i) {
+    const uint32_t b = i & 1, aph = (i >> 1) & 1;
+    if (!wait_bounded(bar(BAR_ACC_EMPTY + b), aph ^ 1, wd)) goto done;
+    tc_fence_after_sync();
+    {
+      const uint32_t d_tmem = tmem_base + b * BN;
+      for (int kb = 0; kb < p.num_kb; ++kb) {
+        const uint32_t s = g % STAGES;
+        if (!wait_bounded(bar(BAR_FULL + s), (g / STAGES) & 1, wd)) goto done;
+        tc_fence_after_sync();
+        const uint32_t a_addr = sbase + OFF_A + s * A_STAGE_BYTES;
+        const uint32_t b_addr = sbase + OFF_B + s * B_STAGE_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < BK / UMMA_K; ++kk) {
+          umma_bf16(d_tmem, sdesc_kmajor_sw128(a_addr + kk * UMMA_K * 2),
+                    sdesc_kmajor_sw128(b_addr + kk * UMMA_K * 2), idesc,
+                    (kb | kk) != 0 ? 1u : 0u);
+        }
+        issued = true;
+        umma_commit(bar(BAR_EMPTY + s));   // stage s free once these MMAs finish
+        ++g;
+      }
+    }
+    if (p.num_kb > 0)
+      umma_commit(bar(BAR_ACC_FULL + b));   // accumulator b complete
+    else
+      mbar_arrive(bar(BAR_ACC_FULL + b));   // K == 0: nothing to wait for
+  }
+done:
+  if (issued) {
+    // Every MMA this thread issued has finished once this arrives; TMEM can
+    // then be freed even on the abort path.
+    umma_commit(bar(BAR_MMA_DRAIN));
+    wait_drain(bar(BAR_MMA_DRAIN), 0);
+  }
+}
+
+// ------------------------------------------------------------ epilogue
+
+__device__ __forceinline__ void unpack_bf16x8(uint4 v, float* f) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = __uint_as_float(w[i] << 16);
+    f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+__device__ __forceinline__ void epilogue_role(const Params& p, uint32_t sbase, uint8_t* smem,
+                                              uint32_t tmem_base, int warp, const Watchdog& wd) {
+  const int lane = threadIdx.x & 31;
+  const int q = warp & 3;   // TMEM lane quarter this warp may access = tile rows 32q..32q+31
+  auto bar = [&](int i) { return sbase + OFF_BAR + 8 * i; };
+  // 64-byte swizzle of a 32-row x 64-byte block: 16-byte chunk c of row r is
+  // stored at chunk c ^ ((r >> 1) & 3); the same pattern TMA uses.
+  const uint32_t row_off = lane * 64;
+  const uint32_t swz = (lane >> 1) & 3;
+  uint32_t u = 0;        // subtiles stored by this warp (D slot ring position)
+  uint32_t cu = 0;       // C subtiles consumed by this warp (C ring position)
+  uint32_t c_issued = 0; // C subtile loads issued by this warp
+  int i = 0;
+  for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++i) {
+    int mb, nb, l;
+    tile_coords(p, t, mb, nb, l);
+    const int m0 = mb * BM + 32 * q, n0 = nb * BN;
+    const int nsub = staging_in_tile(p, nb) * SUB_PER_STAGING;
+    const uint32_t b = i & 1, aph = (i >> 1) & 1;
+
+    auto issue_c = [&](int j) {
+      const uint32_t idx = c_issued++;
+      if (lane == 0) {
+        const uint32_t cb = idx % C_BUFS;
+        const uint32_t cbar = bar(BAR_C_FULL + q * C_BUFS + cb);
+        fence_proxy_async_smem();   // earlier generic reads of this buffer come first
+        mbar_arrive_expect_tx(cbar, EPI_QUARTER_BYTES);
+        tma_load_3d(sbase + OFF_C + cb * EPI_SLOT_BYTES + q * EPI_QUARTER_BYTES, &p.tmC, cbar,
+                    n0 + j * EPI_N, m0, l);
+      }
+    };
+    if (p.has_c) issue_c(0);
+
+    if (!warp_wait(bar(BAR_ACC_FULL + b), aph, wd)) break;
+    tc_fence_after_sync();
+    const uint32_t tacc = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + b * BN;
+
+    bool ok = true;
+    for (int j = 0; j < nsub; ++j) {
+      if (p.has_c && j + 1 < nsub) issue_c(j + 1);
+
+      uint32_t acc[32];
+      if (p.num_kb > 0) {
+        tmem_ld_32x32b_x32(tacc + j * EPI_N, acc);
+        tmem_wait_ld();
+      } else {
+#pragma unroll
+        for (int e = 0; e < 32; ++e) acc[e] = 0u;
+      }
+      if (j == nsub - 1) {
+        // Accumulator b fully read: hand it back to the MMA warp.
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(BAR_ACC_EMPTY + b));
+      }
+
+      float v[32];
+#pragma unroll
+      for (int e = 0; e < 32; ++e) v[e] = p.alpha * __uint_as_float(acc[e]);
+      if (p.has_c) {
+        const uint32_t cb = cu % C_BUFS;
+        if (!warp_wait(bar(BAR_C_FULL + q * C_BUFS + cb), (cu / C_BUFS) & 1, wd)) {
+          ok = false;
+          break;
+        }
+        const uint8_t* cbase = smem + OFF_C + cb * EPI_SLOT_BYTES + q * EPI_QUARTER_BYTES + row_off;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const uint4 raw = *reinterpret_cast<const uint4*>(cbase + ((c ^ swz) << 4));
+          float cf[8];
+          unpack_bf16x8(raw, cf);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) v[8 * c + e] = fmaf(p.beta, cf[e], v[8 * c + e]);
+        }
+        ++cu;
+      }
+
+      // Reuse slot u % EPI_SLOTS only when (a) this warp's TMA store from it
+      // has finished reading it and (b) the stream-out consumer released it.
+      const uint32_t slot = u % EPI_SLOTS;
+      if (lane == 0) bulk_wait_read<EPI_SLOTS - 1>();
+      if (p.streamout) {
+        if (!warp_wait(bar(BAR_D_EMPTY + slot), ((u / EPI_SLOTS) & 1) ^ 1, wd)) {
+          ok = false;
+          break;
+        }
+      }
+      __syncwarp();
+      uint8_t* dq = smem + OFF_D + slot * EPI_SLOT_BYTES + q * EPI_QUARTER_BYTES;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint4 w;
+        w.x = pack_bf16x2(v[8 * c + 0], v[8 * c + 1]);
+        w.y = pack_bf16x2(v[8 * c + 2], v[8 * c + 3]);
+        w.z = pack_bf16x2(v[8 * c + 4], v[8 * c + 5]);
+        w.w = pack_bf16x2(v[8 * c + 6], v[8 * c + 7]);
+        *reinterpret_cast<uint4*>(dq + row_off + ((c ^ swz) << 4)) = w;
+      }
+      fence_proxy_async_smem();   // generic writes -> visible to the TMA (async proxy)
+      __syncwarp();
+      if (lane == 0) {
+        tma_store_3d(&p.tmD, smem_addr(dq), n0 + j * EPI_N, m0, l);
+        bulk_commit();
+        if (p.streamout) mbar_arrive(bar(BAR_D_FULL + slot));
+      }
+      ++u;
+    }
+    if (!ok) break;
+  }
+  if (lane == 0) {
+    // C loads still in flight only after an abort: let them land first.
+    for (uint32_t idx = cu; idx < c_issued; ++idx)
+      wait_drain(bar(BAR_C_FULL + q * C_BUFS + idx % C_BUFS), (idx / C_BUFS) & 1);
+    bulk_wait<0>();   // store tail: every D write has landed
+  }
+  __syncwarp();
+}
+
+// ------------------------------------------------------------ stream-out consumer
+
+__device__ __forceinline__ void consumer_role(const Params& p, uint32_t sbase,
+                                              const Watchdog& wd) {
+  auto bar = [&](int i) { return sbase + OFF_BAR + 8 * i; };
+  uint32_t u = 0;
+  for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
+    int mb, nb, l;
+    tile_coords(p, t, mb, nb, l);
+    const int nst = staging_in_tile(p, nb);
+    for (int st = 0; st < nst; ++st) {
+      const int tile_id = (l * p.tiles_m + mb) * p.staging_tiles_n + nb * (BN / STAGING) + st;
+      uint32_t seq = 0;
+      for (int jj = 0; jj < SUB_PER_STAGING; ++jj) {
+        const uint32_t slot = u % EPI_SLOTS;
+        if (!wait_bounded(bar(BAR_D_FULL + slot), (u / EPI_SLOTS) & 1, wd)) goto done;
+        if (jj == 0) seq = atomicAdd(p.counter, 1u);   // completion order
+        tma_store_3d(&p.tmS, sbase + OFF_D + slot * EPI_SLOT_BYTES, jj * EPI_N, 0,
+                     static_cast<int>(seq));
+        bulk_commit();
+        bulk_wait_read<0>();                  // slot read: give it back
+        mbar_arrive(bar(BAR_D_EMPTY + slot));
+        ++u;
+      }
+      bulk_wait<0>();                         // staging bytes written
+      fence_proxy_async_global();
+      __threadfence();
+      st_relaxed_gpu(p.flags + 2 * tile_id, seq);
+      st_release_gpu(p.flags + 2 * tile_id + 1, 1u);
+    }
+  }
+done:
+  bulk_wait<0>();
+}
+
+// ------------------------------------------------------------ kernel
+
+__global__ void __launch_bounds__(NUM_THREADS, 1) gemm_ws_kernel(const __grid_constant__ Params p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  const uint32_t raw = smem_addr(smem_raw);
+  const uint32_t pad = ((raw + 1023u) & ~1023u) - raw;
+  uint8_t* smem = smem_raw + pad;
+  const uint32_t sbase = raw + pad;
+  const int warp = __shfl_sync(0xffffffffu, static_cast<int>(threadIdx.x / 32), 0);
+  const int lane = threadIdx.x & 31;
+  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + OFF_ABORT);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_TMEM_SLOT);
+
+  if (warp == WARP_TMA && lane == 0) {
+    auto bar = [&](int i) { return sbase + OFF_BAR + 8 * i; };
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(bar(BAR_FULL + s), 1);
+      mbar_init(bar(BAR_EMPTY + s), 1);
+    }
+    for (int b = 0; b < ACC_BUFS; ++b) {
+      mbar_init(bar(BAR_ACC_FULL + b), 1);
+      mbar_init(bar(BAR_ACC_EMPTY + b), NUM_EPI_WARPS);
+    }
+    for (int i = 0; i < NUM_EPI_WARPS * C_BUFS; ++i) mbar_init(bar(BAR_C_FULL + i), 1);
+    for (int s = 0; s < EPI_SLOTS; ++s) {
+      mbar_init(bar(BAR_D_FULL + s), NUM_EPI_WARPS);
+      mbar_init(bar(BAR_D_EMPTY + s), 1);
+    }
+    mbar_init(bar(BAR_MMA_DRAIN), 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    if (p.num_kb > 0) {
+      prefetch_tensormap(&p.tmA);
+      prefetch_tensormap(&p.tmB);
+    }
+    if (p.has_c) prefetch_tensormap(&p.tmC);
+    prefetch_tensormap(&p.tmD);
+    if (p.streamout) prefetch_tensormap(&p.tmS);
+  }
+  if (warp == WARP_MMA) {
+    tmem_alloc(smem_addr(tmem_slot), TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
+  const Watchdog wd{abort_flag, p.status, p.timeout_ns};
+
+  if (warp == WARP_TMA) {
+    if (lane == 0) producer_role(p, sbase, wd);
+  } else if (warp == WARP_MMA) {
+    if (lane == 0) mma_role(p, sbase, tmem_base, wd);
+  } else if (warp < WARP_EPI0 + NUM_EPI_WARPS) {
+    epilogue_role(p, sbase, smem, tmem_base, warp, wd);
+  } else if (warp == WARP_CONSUMER && p.streamout) {
+    if (lane == 0) consumer_role(p, sbase, wd);
+  }
+
+  __syncwarp();
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == WARP_MMA) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+}  // namespace gws

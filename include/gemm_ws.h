@@ -1,0 +1,121 @@
+/*
+ * gemm_ws.h — C ABI of the GB300 (sm_103a) persistent warp-specialized GEMM
+ *
+ *   D[l] = alpha * A[l] * B[l] + beta * C[l]      for l = 0 .. L-1
+ *
+ * bf16 operands, fp32 accumulation in tensor memory, bf16 output.
+ *
+ * Where the operation is defined:
+ *  - "sm90_gemm_tma_warpspecialized_cooperative.hpp" (CUTLASS kernel layer):
+ *    the MNKL problem shape (rank-4 problem with an appended batch mode L),
+ *    the host-side `can_implement` / workspace conventions, and the epilogue
+ *    that reads C and writes D = alpha * accumulator + beta * C;
+ *  - "How to build a pipeline between epilogue and communication warp
+ *    groups?" (CUTLASS issue): the per-tile producer/consumer handoff from
+ *    the epilogue to a separate consumer warp, which this library implements
+ *    as the stream-out consumer (gemm_ws_run_streamout);
+ *  - "why does load() pre-issue producer_try_acquire for the next stage"
+ *    (CUTLASS discussion): the TMA producer's early try-acquire.
+ *
+ * Layouts (all packed, no padding between batches):
+ *  - A: L x M x K row-major (K contiguous);
+ *  - B: column-major K x N per batch, i.e. stored L x N x K with K contiguous;
+ *  - C, D: L x M x N row-major.
+ * Element type: IEEE bfloat16 bit patterns (uint16_t).
+ *
+ * Ownership: every data pointer is a borrowed DEVICE pointer on the handle's
+ * device; the caller owns it and keeps it alive until the stream work ends.
+ * The handle owns only its small device workspace (stream-out counter and
+ * status word).
+ *
+ * Errors: every entry point returns a gemm_ws_status. A call that returns an
+ * error other than GEMM_WS_ERR_CUDA launched nothing and wrote nothing. All
+ * runs are asynchronous on `stream` (a cudaStream_t passed as void*, NULL
+ * meaning the legacy default stream); device-side problems (a watchdog
+ * timeout) are reported by gemm_ws_query_status.
+ */
+#ifndef GEMM_WS_H_
+#define GEMM_WS_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum gemm_ws_status {
+  GEMM_WS_OK = 0,
+  GEMM_WS_ERR_INVALID_ARG = 1, /* NULL pointer, negative size, beta != 0 with C NULL,
+                                  D aliasing A or B, a size beyond the limits below */
+  GEMM_WS_ERR_ALIGNMENT = 2,   /* a pointer not 16-byte aligned, or K or N not a
+                                  multiple of 8 (TMA needs 16-byte row pitches) */
+  GEMM_WS_ERR_UNSUPPORTED = 3, /* device is not sm_103 (GB300) */
+  GEMM_WS_ERR_CUDA = 4,        /* a CUDA runtime/driver call failed; see
+                                  gemm_ws_last_cuda_error */
+  GEMM_WS_ERR_TIMEOUT = 5      /* a bounded on-device wait gave up (watchdog) */
+} gemm_ws_status;
+
+typedef struct gemm_ws gemm_ws_t;
+
+/* Creates a handle bound to CUDA device `device`: checks that it is sm_103,
+ * queries its SM count, allocates the device workspace and sets the kernel's
+ * shared-memory attribute. The caller owns *out and frees it with
+ * gemm_ws_destroy. On error *out is set to NULL. */
+int gemm_ws_create(gemm_ws_t** out, int device);
+
+/* Frees the handle and its workspace (synchronising the device first). NULL
+ * is accepted and ignored. */
+int gemm_ws_destroy(gemm_ws_t* h);
+
+/* D[l] = alpha * A[l] * B[l] + beta * C[l], asynchronously on `stream`.
+ *  - A: L*M*K, B: L*N*K, C: L*M*N (may be NULL iff beta == 0, in which case C
+ *    is never read), D: L*M*N; all bf16, layouts as above.
+ *  - M, N, K, L >= 0, each < 2^31, and L*M*N, L*M*K, L*N*K < 2^40.
+ *  - K % 8 == 0 and N % 8 == 0 (16-byte row pitches); pointers 16-byte aligned.
+ *  - K == 0 gives D = beta * C (or 0); M*N*L == 0 launches nothing.
+ *  - D must not overlap A or B; D may be exactly C (in place).
+ * Rounding: fp32 alpha * acc + beta * c, then round-to-nearest-even to bf16. */
+int gemm_ws_run(gemm_ws_t* h, const uint16_t* A, const uint16_t* B,
+                const uint16_t* C, uint16_t* D, int64_t M, int64_t N, int64_t K,
+                int64_t L, float alpha, float beta, void* stream);
+
+/* gemm_ws_run plus tile stream-out: a consumer warp takes every finished
+ * 128 x 128 output tile from the epilogue through an on-chip full/empty
+ * handoff and copies it into `staging`, in the order it takes the tiles.
+ *  - T = L * ceil(M/128) * ceil(N/128) output tiles; tile index
+ *    t = (l * ceil(M/128) + m_tile) * ceil(N/128) + n_tile.
+ *  - staging: device buffer of T * 128 * 128 bf16; slot s holds, row-major
+ *    128 x 128, the tile that was taken s-th; elements of an edge tile outside
+ *    M or N are 0.
+ *  - flags: device buffer of 2 * T uint32. After the stream work completes,
+ *    flags[2t] = s (the slot / sequence number of tile t, 0-based and dense)
+ *    and flags[2t+1] = 1. The library clears flags on `stream` before the
+ *    launch; the ready word is written with release semantics after the
+ *    tile's staging bytes are globally visible.
+ *  - staging and flags must not overlap any other argument.
+ * Returns as gemm_ws_run. */
+int gemm_ws_run_streamout(gemm_ws_t* h, const uint16_t* A, const uint16_t* B,
+                          const uint16_t* C, uint16_t* D, int64_t M, int64_t N,
+                          int64_t K, int64_t L, float alpha, float beta,
+                          uint16_t* staging, uint32_t* flags, void* stream);
+
+/* Synchronises `stream` and returns the device status word of the handle:
+ * GEMM_WS_OK, or GEMM_WS_ERR_TIMEOUT if a run's bounded wait gave up (the
+ * run's outputs are then undefined). Reading clears the word. */
+int gemm_ws_query_status(gemm_ws_t* h, void* stream);
+
+/* The last CUDA error code (cudaError_t value) seen by this handle, 0 if none. */
+int gemm_ws_last_cuda_error(gemm_ws_t* h);
+
+/* A static, human-readable name for a gemm_ws_status value. */
+const char* gemm_ws_status_string(int status);
+
+/* Output tiles (128 x 128) of an M x N x L problem: the T of
+ * gemm_ws_run_streamout. Pure host arithmetic; needs no GPU. */
+int64_t gemm_ws_streamout_tiles(int64_t M, int64_t N, int64_t L);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GEMM_WS_H_ */

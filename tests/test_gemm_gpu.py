@@ -1,0 +1,200 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle.
+
+Tolerance (per element): |d - ref| <= ulp_bf16(ref) + 1e-3 * sqrt(K / 64).
+Integer-valued inputs make the fp32 accumulation exact, so there the bf16
+result must equal the oracle rounded to bf16 bit for bit.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from async_pipelines_gb300 import gemm_ws, workloads
+from tests.gpu_helpers import bits_of, sample_rows, to_dev
+from tests.numerics import assert_gemm_close, f64_to_bf16_bits
+from tests.test_oracle import load_handworked
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def gw():
+    g = gemm_ws.GemmWS(0)
+    yield g
+    assert g.query_status() == gemm_ws.OK
+    g.close()
+
+
+def run_case(gw, M, N, K, L, alpha, beta, ab=("uniform",), cd=None, seed=0, rows=None,
+             streamout=False):
+    """Runs one GEMM on the GPU; returns (D bits, oracle rows, rows or None)."""
+    A, B, C = workloads.make_inputs(M, N, K, L, ab, cd, seed)
+    Ad, Bd, Cd = to_dev(A), to_dev(B), to_dev(C)
+    D = torch.empty(L, M, N, dtype=torch.bfloat16, device="cuda")
+    gw.run(Ad, Bd, Cd, D, alpha, beta)
+    torch.cuda.synchronize()
+    ref = oracle.gemm_rows(bits_of(A), bits_of(B), None if C is None else bits_of(C),
+                           M, N, K, L, alpha, beta, rows=rows)
+    d = bits_of(D).reshape(L * M, N)
+    if rows is not None:
+        d = d[rows]
+    return d, ref
+
+
+# ------------------------------------------------------------------ exact cases
+
+def test_handworked_fixture(gw):
+    """The hand-worked 2x3x4 example, zero-padded to K = N = 8 (16-byte rows)."""
+    A, Bkn, C, Dexp, alpha, beta = load_handworked()
+    M, K = A.shape
+    N = Bkn.shape[1]
+    Ap = np.zeros((M, 8)); Ap[:, :K] = A
+    Bp = np.zeros((8, 8)); Bp[:N, :K] = Bkn.T          # stored N x K
+    Cp = np.zeros((M, 8)); Cp[:, :N] = C
+    t = lambda x: torch.from_numpy(f64_to_bf16_bits(x).astype(np.int16)).view(
+        torch.bfloat16).reshape(1, *x.shape).cuda()
+    D = torch.empty(1, M, 8, dtype=torch.bfloat16, device="cuda")
+    gw.run(t(Ap), t(Bp), t(Cp), D, alpha, beta)
+    torch.cuda.synchronize()
+    got = bits_of(D).reshape(M, 8)
+    np.testing.assert_array_equal(got[:, :N], f64_to_bf16_bits(Dexp))
+    np.testing.assert_array_equal(got[:, N:], 0)
+
+
+@pytest.mark.parametrize("M,N,K,L", [
+    (128, 256, 64, 1),      # exactly one tile, one k-block
+    (300, 520, 200, 2),     # ragged M, N, K; several tiles; batches
+    (1, 8, 8, 1),           # smallest legal problem
+    (2048, 2048, 128, 1),   # more tiles than SMs: persistent loop, ring wraps
+])
+def test_integer_inputs_bit_exact(gw, M, N, K, L):
+    A, B, C = workloads.make_inputs(M, N, K, L, ("int", -4, 4), ("int", -4, 4), seed=M + K)
+    D = torch.empty(L, M, N, dtype=torch.bfloat16, device="cuda")
+    gw.run(to_dev(A), to_dev(B), to_dev(C), D, 2.0, -3.0)
+    torch.cuda.synchronize()
+    ref = oracle.gemm(bits_of(A), bits_of(B), bits_of(C), M, N, K, L, 2.0, -3.0)
+    np.testing.assert_array_equal(bits_of(D).reshape(L, M, N), f64_to_bf16_bits(ref))
+
+
+# ------------------------------------------------------------------ small shapes
+
+@pytest.mark.parametrize("M,N,K,L,alpha,beta", [
+    (256, 256, 256, 1, 1.0, 0.0),
+    (200, 136, 72, 1, 1.0, 0.0),      # ragged edges, K not a multiple of 64
+    (130, 264, 8, 3, 1.5, 0.5),       # K < 64, batches, C
+    (64, 512, 56, 2, -1.25, 0.75),
+    (513, 1032, 1000, 1, 1.0, 1.0),
+    (4096, 4096, 128, 1, 1.0, 0.0),   # 512 tiles: several tiles per CTA
+])
+def test_small_shapes_match_oracle(gw, M, N, K, L, alpha, beta):
+    cd = ("normal", 1.0) if beta != 0 else None
+    d, ref = run_case(gw, M, N, K, L, alpha, beta, cd=cd, seed=17)
+    assert_gemm_close(d, ref, K, f"{M}x{N}x{K}x{L}")
+
+
+def test_k_zero_gives_beta_c(gw):
+    M, N, L = 200, 264, 2
+    C = workloads.make_inputs(M, N, 0, L, ("uniform",), ("uniform",), 3)[2]
+    D = torch.full((L, M, N), 7.0, dtype=torch.bfloat16, device="cuda")
+    A = torch.empty(L, M, 0, dtype=torch.bfloat16, device="cuda")
+    B = torch.empty(L, N, 0, dtype=torch.bfloat16, device="cuda")
+    gw.run(A, B, C.cuda(), D, 1.0, 0.5)
+    torch.cuda.synchronize()
+    ref = oracle.gemm(np.zeros(0, np.uint16), np.zeros(0, np.uint16), bits_of(C),
+                      M, N, 0, L, 1.0, 0.5)
+    assert_gemm_close(bits_of(D), ref, 0, "K=0")
+
+
+def test_beta_zero_ignores_nan_c(gw):
+    M, N, K, L = 192, 256, 128, 1
+    A, B, _ = workloads.make_inputs(M, N, K, L, ("uniform",), None, 5)
+    C = torch.full((L, M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+    D = torch.empty(L, M, N, dtype=torch.bfloat16, device="cuda")
+    gw.run(A.cuda(), B.cuda(), C, D, 1.0, 0.0)
+    torch.cuda.synchronize()
+    ref = oracle.gemm(bits_of(A), bits_of(B), None, M, N, K, L, 1.0, 0.0)
+    assert_gemm_close(bits_of(D), ref, K, "beta=0 with NaN C")
+
+
+def test_in_place_d_is_c(gw):
+    M, N, K, L = 320, 392, 96, 2
+    A, B, C = workloads.make_inputs(M, N, K, L, ("uniform",), ("normal", 1.0), 9)
+    D = C.clone().cuda()
+    gw.run(A.cuda(), B.cuda(), D, D, 1.0, -1.0)
+    torch.cuda.synchronize()
+    ref = oracle.gemm(bits_of(A), bits_of(B), bits_of(C), M, N, K, L, 1.0, -1.0)
+    assert_gemm_close(bits_of(D), ref, K, "D is C")
+
+
+def test_empty_problem_is_a_no_op(gw):
+    D = torch.full((1, 0, 8), 1.0, dtype=torch.bfloat16, device="cuda")
+    A = torch.empty(1, 0, 8, dtype=torch.bfloat16, device="cuda")
+    B = torch.empty(1, 8, 8, dtype=torch.bfloat16, device="cuda")
+    gw.run(A, B, None, D, 1.0, 0.0)
+    D2 = torch.full((2, 16, 8), 3.0, dtype=torch.bfloat16, device="cuda")
+    B0 = torch.empty(2, 8, 8, dtype=torch.bfloat16, device="cuda")
+    A0 = torch.empty(2, 16, 8, dtype=torch.bfloat16, device="cuda")
+    # N == 0 problem: D has no elements; nothing launches
+    rc = gemm_ws.gemm_ws_run(gw.handle, A0, B0, None, D2, 16, 0, 8, 2, 1.0, 0.0)
+    assert rc == gemm_ws.OK
+    torch.cuda.synchronize()
+    assert torch.all(D2 == 3.0)
+
+
+def test_repeated_runs_are_identical(gw):
+    """Shakes out mbarrier phase bugs: many back-to-back launches, same bits."""
+    M, N, K, L = 640, 1280, 320, 1
+    A, B, _ = workloads.make_inputs(M, N, K, L, ("uniform",), None, 21)
+    Ad, Bd = A.cuda(), B.cuda()
+    first = torch.empty(L, M, N, dtype=torch.bfloat16, device="cuda")
+    gw.run(Ad, Bd, None, first, 1.0, 0.0)
+    D = torch.empty_like(first)
+    for _ in range(30):
+        gw.run(Ad, Bd, None, D, 1.0, 0.0)
+    torch.cuda.synchronize()
+    assert torch.equal(first.view(torch.int16), D.view(torch.int16))
+    ref = oracle.gemm(bits_of(A), bits_of(B), None, M, N, K, L, 1.0, 0.0)
+    assert_gemm_close(bits_of(D), ref, K, "repeat")
+
+
+# ------------------------------------------------------------------ argument checks
+
+def test_argument_errors_launch_nothing(gw):
+    h = gw.handle
+    A = torch.zeros(1, 64, 64, dtype=torch.bfloat16, device="cuda")
+    B = torch.zeros(1, 64, 64, dtype=torch.bfloat16, device="cuda")
+    D = torch.full((1, 64, 64), 5.0, dtype=torch.bfloat16, device="cuda")
+    run = gemm_ws.gemm_ws_run
+    assert run(h, A, B, None, D, 64, 64, 64, 1, 1.0, 1.0) == gemm_ws.ERR_INVALID_ARG  # C NULL
+    assert run(h, A, B, None, D, -1, 64, 64, 1, 1.0, 0.0) == gemm_ws.ERR_INVALID_ARG
+    assert run(h, A, B, None, None, 64, 64, 64, 1, 1.0, 0.0) == gemm_ws.ERR_INVALID_ARG
+    assert run(h, A, B, None, A, 64, 64, 64, 1, 1.0, 0.0) == gemm_ws.ERR_INVALID_ARG  # D is A
+    assert run(h, A, B, None, D, 64, 64, 60, 1, 1.0, 0.0) == gemm_ws.ERR_ALIGNMENT   # K % 8
+    assert run(h, A, B, None, D, 64, 60, 64, 1, 1.0, 0.0) == gemm_ws.ERR_ALIGNMENT   # N % 8
+    Dv = D.view(-1)[1:].view(-1)                                                    # 2-byte offset
+    assert gemm_ws.load_library().gemm_ws_run(
+        h, A.data_ptr(), B.data_ptr(), None, Dv.data_ptr(), 8, 8, 64, 1, 1.0, 0.0,
+        torch.cuda.current_stream().cuda_stream) == gemm_ws.ERR_ALIGNMENT
+    torch.cuda.synchronize()
+    assert torch.all(D == 5.0)
+
+
+# ------------------------------------------------------------------ full-size workloads
+
+@pytest.mark.parametrize("name", [
+    "gemm_256x256x256",
+    "gemm_4096x4096x4096",
+    "gemm_8192x8192x8192_alpha_beta",
+    "gemm_batched4_5000x3000x4000_ragged",
+])
+def test_workload_parity(gw, name):
+    """Each workload at full size, in the launch configuration the benchmark
+    times; the oracle computes every row of the small case and sampled rows
+    (edges of every batch and tile band plus random rows) of the big ones."""
+    w = workloads.WORKLOADS[name]
+    rows = None if w.M * w.L <= 512 else sample_rows(w.M, w.L, 48, seed=w.seed)
+    d, ref = run_case(gw, w.M, w.N, w.K, w.L, w.alpha, w.beta, ab=w.ab_dist, cd=w.c_dist,
+                      seed=w.seed, rows=rows)
+    assert_gemm_close(d, ref, w.K, name)
