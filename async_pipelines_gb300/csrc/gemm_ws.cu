@@ -9,6 +9,7 @@
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
+#include <mutex>
 
 #include "gemm_ws.h"
 #include "gemm_ws_kernel.cuh"
@@ -288,3 +289,106 @@ int64_t gemm_ws_streamout_tiles(int64_t M, int64_t N, int64_t L) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Allocation-free stream-out entry point.
+//
+// For callers that must not allocate device memory themselves or through the
+// library: code running where cudaMalloc is unavailable or forbidden (inside
+// another allocator's callback, under a framework that owns every device
+// allocation and pools it, or in a process that reserved all memory up
+// front). gemm_ws_create needs cudaMalloc for its workspace; this entry point
+// needs no handle. Its only scratch (the stream-out sequence counter and the
+// watchdog status word) lives in the fixed array below, which every GPU that
+// loads this library holds until the process exits.
+
+namespace {
+
+constexpr int kNoAllocScratchWords = 64;   // 256 bytes per device; 2 words used
+constexpr int kNoAllocMaxDevices = 64;
+
+struct NoAllocDevice {
+  bool ready;
+  int num_sms;
+  uint32_t* scratch;   // device address of g_noalloc_scratch on this device
+  unsigned long long timeout_ns;
+  PFN_cuTensorMapEncodeTiled_v12000 encode;
+};
+
+NoAllocDevice g_noalloc_devices[kNoAllocMaxDevices];
+std::mutex g_noalloc_mutex;
+
+}  // namespace
+
+// word 0: stream-out sequence counter; word 1: watchdog status.
+static __device__ __align__(256) uint32_t g_noalloc_scratch[kNoAllocScratchWords];
+
+namespace {
+
+// Once per device, with that device current: checks it is sm_103, reads its
+// SM count, sets the kernel's shared-memory attribute, fetches the tensor-map
+// encoder and takes the device address of the scratch array. Allocates
+// nothing.
+int noalloc_setup(int device, NoAllocDevice** out) {
+  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+  NoAllocDevice& d = g_noalloc_devices[device];
+  if (!d.ready) {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, device) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, device) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess)
+      return GEMM_WS_ERR_CUDA;
+    if (major != 10 || minor != 3) return GEMM_WS_ERR_UNSUPPORTED;
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !fn)
+      return GEMM_WS_ERR_CUDA;
+    if (cudaFuncSetAttribute(gws::gemm_ws_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(gws::SMEM_BYTES)) != cudaSuccess)
+      return GEMM_WS_ERR_CUDA;
+    uint32_t* ptr = nullptr;
+    // In host code the array's name is only a host-side stand-in; the kernel
+    // must be given this device address instead.
+    if (cudaGetSymbolAddress(reinterpret_cast<void**>(&ptr), g_noalloc_scratch) != cudaSuccess ||
+        !ptr)
+      return GEMM_WS_ERR_CUDA;
+    d.timeout_ns = 1000000000ull;
+    if (const char* s = std::getenv("GEMM_WS_TIMEOUT_MS")) {
+      const long long ms = std::atoll(s);
+      if (ms > 0) d.timeout_ns = static_cast<unsigned long long>(ms) * 1000000ull;
+    }
+    d.num_sms = sms;
+    d.scratch = ptr;
+    d.encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    d.ready = true;
+  }
+  *out = &d;
+  return GEMM_WS_OK;
+}
+
+}  // namespace
+
+extern "C" int gemm_ws_run_streamout_noalloc(const uint16_t* A, const uint16_t* B,
+                                             const uint16_t* C, uint16_t* D, int64_t M,
+                                             int64_t N, int64_t K, int64_t L, float alpha,
+                                             float beta, uint16_t* staging, uint32_t* flags,
+                                             void* stream) {
+  int device = -1;
+  if (cudaGetDevice(&device) != cudaSuccess) return GEMM_WS_ERR_CUDA;
+  if (device < 0 || device >= kNoAllocMaxDevices) return GEMM_WS_ERR_INVALID_ARG;
+  // The sequence counter in the scratch numbers tiles with 31 bits.
+  if (gemm_ws_streamout_tiles(M, N, L) > kMaxDim) return GEMM_WS_ERR_INVALID_ARG;
+  NoAllocDevice* d = nullptr;
+  int rc = noalloc_setup(device, &d);
+  if (rc != GEMM_WS_OK) return rc;
+  gemm_ws h;   // a handle on the host stack that borrows the static scratch
+  std::memset(&h, 0, sizeof h);
+  h.device = device;
+  h.num_sms = d->num_sms;
+  h.work = d->scratch;
+  h.timeout_ns = d->timeout_ns;
+  h.encode = d->encode;
+  return gemm_ws_run_streamout(&h, A, B, C, D, M, N, K, L, alpha, beta, staging, flags, stream);
+}

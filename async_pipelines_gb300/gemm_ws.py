@@ -25,7 +25,7 @@ ERR_TIMEOUT = 5
 EXPORTS = (
     "gemm_ws_create", "gemm_ws_destroy", "gemm_ws_run", "gemm_ws_run_streamout",
     "gemm_ws_query_status", "gemm_ws_last_cuda_error", "gemm_ws_status_string",
-    "gemm_ws_streamout_tiles",
+    "gemm_ws_streamout_tiles", "gemm_ws_run_streamout_noalloc",
 )
 
 STAGING_TILE = 128
@@ -64,6 +64,8 @@ def load_library(path: Optional[str] = None):
     lib.gemm_ws_run.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, f32, f32, vp]
     lib.gemm_ws_run_streamout.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, f32, f32,
                                           vp, vp, vp]
+    lib.gemm_ws_run_streamout_noalloc.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, f32, f32,
+                                                  vp, vp, vp]
     lib.gemm_ws_query_status.argtypes = [vp, vp]
     lib.gemm_ws_last_cuda_error.argtypes = [vp]
     lib.gemm_ws_status_string.argtypes = [ctypes.c_int]
@@ -71,7 +73,8 @@ def load_library(path: Optional[str] = None):
     lib.gemm_ws_streamout_tiles.argtypes = [i64, i64, i64]
     lib.gemm_ws_streamout_tiles.restype = i64
     for name in ("gemm_ws_create", "gemm_ws_destroy", "gemm_ws_run", "gemm_ws_run_streamout",
-                 "gemm_ws_query_status", "gemm_ws_last_cuda_error"):
+                 "gemm_ws_query_status", "gemm_ws_last_cuda_error",
+                 "gemm_ws_run_streamout_noalloc"):
         getattr(lib, name).restype = ctypes.c_int
     if path is None:
         _lib = lib
@@ -122,6 +125,15 @@ def gemm_ws_run_streamout(h, A, B, C, D, M, N, K, L, alpha, beta, staging, flags
                           stream=None) -> int:
     return load_library().gemm_ws_run_streamout(
         h, _ptr(A), _ptr(B), _ptr(C), _ptr(D), M, N, K, L, float(alpha), float(beta),
+        _ptr(staging), _ptr(flags), _stream(stream))
+
+
+def gemm_ws_run_streamout_noalloc(A, B, C, D, M, N, K, L, alpha, beta, staging, flags,
+                                  stream=None) -> int:
+    """Stream-out GEMM on the current device with no handle and no device
+    allocation (its scratch is a fixed array inside the library)."""
+    return load_library().gemm_ws_run_streamout_noalloc(
+        _ptr(A), _ptr(B), _ptr(C), _ptr(D), M, N, K, L, float(alpha), float(beta),
         _ptr(staging), _ptr(flags), _stream(stream))
 
 

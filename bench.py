@@ -115,7 +115,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=self.out, stderr=subprocess.DEVNULL)
         except (OSError, ValueError):
             self.proc = None
@@ -328,6 +328,36 @@ def run_ours(args, rank, world, local):
     print(json.dumps(line), flush=True)
 
 
+def run_kernel_only(args, local):
+    """Only the GEMM launches of one workload (warmup + steps), for profilers."""
+    from async_pipelines_gb300 import gemm_ws
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    g = gemm_ws.GemmWS(local)
+    w = workloads.WORKLOADS[args.workload or workloads.HEADLINE]
+    A, B, C = workloads.workload_inputs(w)
+    Ad, Bd = A.to(dev), B.to(dev)
+    Cd = C.to(dev) if C is not None else None
+    D = torch.empty(w.L, w.M, w.N, dtype=torch.bfloat16, device=dev)
+    if w.streamout:
+        T = gemm_ws.gemm_ws_streamout_tiles(w.M, w.N, w.L)
+        staging = torch.empty(T * 128 * 128, dtype=torch.bfloat16, device=dev)
+        flags = torch.empty(2 * T, dtype=torch.int32, device=dev)
+        step = lambda: g.run_streamout(Ad, Bd, Cd, D, staging, flags, w.alpha, w.beta)
+    else:
+        step = lambda: g.run(Ad, Bd, Cd, D, w.alpha, w.beta)
+    for _ in range(args.warmup):
+        step()
+    ms = time_launches(step, args.steps, torch.cuda.current_stream())
+    status = g.query_status()
+    g.close()
+    if status != gemm_ws.OK:
+        raise RuntimeError(f"device status: {gemm_ws.status_string(status)}")
+    print(json.dumps({"workload": w.name, "ms_per_launch": round(ms, 4),
+                      "tflops": round(w.flops / (ms * 1e-3) / 1e12, 2)}), flush=True)
+
+
 def run_reference(args, rank, world, local):
     """The reference arm: the CPU oracle, timed on this host's cores."""
     if rank != 0:
@@ -369,19 +399,25 @@ def run_reference(args, rank, world, local):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-budget", type=float, default=15.0,
                     help="seconds of CPU oracle work for the baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--overhead-reps", type=int, default=30)
+    ap.add_argument("--kernel-only", action="store_true",
+                    help="launch only the GEMM of --workload (for profilers); no contract line")
+    ap.add_argument("--workload", choices=sorted(workloads.WORKLOADS), default=None)
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     rank, world, local = dist_env()
     if args.impl == "reference":
         run_reference(args, rank, world, local)
+        return
+    if args.kernel_only:
+        run_kernel_only(args, local)
         return
     if world > 1:
         import torch.distributed as dist

@@ -114,6 +114,36 @@ const char* gemm_ws_status_string(int status);
  * gemm_ws_run_streamout. Pure host arithmetic; needs no GPU. */
 int64_t gemm_ws_streamout_tiles(int64_t M, int64_t N, int64_t L);
 
+/* gemm_ws_run_streamout for callers that cannot allocate device memory.
+ *
+ * No counterpart on the pages: this is a library convenience. Some callers
+ * may not call cudaMalloc (code that runs inside another allocator's hook, a
+ * framework that owns and pools every device allocation, a process that
+ * reserved all device memory up front), so they cannot create the handle,
+ * whose workspace is cudaMalloc'ed. This call needs no handle and allocates
+ * nothing: it runs on the CURRENT device, and its scratch (the 32-bit
+ * stream-out sequence counter and the watchdog status word) is a fixed
+ * 256-byte array in the library's device memory, which every GPU that loads
+ * the library holds until the process exits.
+ *  - Arguments, layouts, results and errors are those of
+ *    gemm_ws_run_streamout. A problem of more than 2^31 - 1 stream-out tiles
+ *    (beyond what the scratch counter numbers) returns
+ *    GEMM_WS_ERR_INVALID_ARG.
+ *  - The first call on a device does a one-time set-up there (device
+ *    checks, kernel attribute, address of the scratch array); make that first
+ *    call before any stream capture.
+ *  - Every call shares the one scratch array, which keeps the last call's
+ *    contents; each call clears the counter (and the flags) on `stream`
+ *    before its launch. Calls that overlap on the GPU (e.g. on two streams)
+ *    race on the counter and produce wrong sequence numbers: serialise them.
+ *  - A watchdog timeout is not reported through a status query here; it shows
+ *    as tiles whose ready word flags[2t+1] stayed 0. */
+int gemm_ws_run_streamout_noalloc(const uint16_t* A, const uint16_t* B,
+                                  const uint16_t* C, uint16_t* D, int64_t M,
+                                  int64_t N, int64_t K, int64_t L, float alpha,
+                                  float beta, uint16_t* staging, uint32_t* flags,
+                                  void* stream);
+
 #ifdef __cplusplus
 }
 #endif
