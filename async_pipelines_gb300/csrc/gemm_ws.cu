@@ -17,6 +17,9 @@
 struct gemm_ws {
   int device;
   int num_sms;
+  int cta_group;                  // 2: CTA-pair tiles (default); 1: single-CTA tiles
+  int group_m;                    // raster group: m-tiles walked per n step
+  int max_pair_clusters;          // co-resident 2-CTA clusters of the pair kernel
   uint32_t* work;                 // [0] stream-out counter, [1] status word
   int last_cuda_error;
   unsigned long long timeout_ns;
@@ -77,24 +80,54 @@ int check_problem(gemm_ws* h, const uint16_t* A, const uint16_t* B, const uint16
   return GEMM_WS_OK;
 }
 
+// Sets the shared-memory attribute of both kernel instances on the current
+// device and returns how many 2-CTA clusters of the pair kernel fit at once.
+cudaError_t configure_kernels(int num_sms, int* max_pair_clusters) {
+  cudaError_t e = cudaFuncSetAttribute(gws::gemm_ws_kernel<1>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(gws::Cfg<1>::SMEM_BYTES));
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(gws::gemm_ws_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(gws::Cfg<2>::SMEM_BYTES));
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(2 * (num_sms / 2), 1, 1);
+  cfg.blockDim = dim3(gws::NUM_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = gws::Cfg<2>::SMEM_BYTES;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int clusters = 0;
+  e = cudaOccupancyMaxActiveClusters(&clusters, gws::gemm_ws_kernel<2>, &cfg);
+  if (e != cudaSuccess) return e;
+  *max_pair_clusters = clusters;
+  return cudaSuccess;
+}
+
 int launch(gemm_ws* h, const uint16_t* A, const uint16_t* B, const uint16_t* C, uint16_t* D,
            int64_t M, int64_t N, int64_t K, int64_t L, float alpha, float beta,
            uint16_t* staging, uint32_t* flags, cudaStream_t stream) {
   gws::Params p;
   std::memset(&p, 0, sizeof p);
-  const int64_t tiles_m = (M + gws::BM - 1) / gws::BM;
+  const int cg = h->cta_group;
+  const int64_t tiles_m = (M + gws::BM * cg - 1) / (gws::BM * cg);
   const int64_t tiles_n = (N + gws::BN - 1) / gws::BN;
   const int64_t num_tiles = L * tiles_m * tiles_n;
   if (num_tiles > kMaxDim) return GEMM_WS_ERR_INVALID_ARG;
   const int64_t stn = (N + gws::STAGING - 1) / gws::STAGING;
-  const int64_t T = L * tiles_m * stn;
+  const int64_t T = L * ((M + gws::STAGING - 1) / gws::STAGING) * stn;
+  if (T > kMaxDim) return GEMM_WS_ERR_INVALID_ARG;
 
   CUresult r = CUDA_SUCCESS;
   if (K > 0) {
     r = encode3d(h, &p.tmA, A, K, M, L, gws::BK, gws::BM, CU_TENSOR_MAP_SWIZZLE_128B,
                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
     if (r == CUDA_SUCCESS)
-      r = encode3d(h, &p.tmB, B, K, N, L, gws::BK, gws::BN, CU_TENSOR_MAP_SWIZZLE_128B,
+      r = encode3d(h, &p.tmB, B, K, N, L, gws::BK, gws::BN / cg, CU_TENSOR_MAP_SWIZZLE_128B,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
   }
   if (r == CUDA_SUCCESS && beta != 0.0f)
@@ -120,7 +153,8 @@ int launch(gemm_ws* h, const uint16_t* A, const uint16_t* B, const uint16_t* C, 
   p.tiles_n = static_cast<int>(tiles_n);
   p.num_tiles = static_cast<int>(num_tiles);
   p.num_kb = static_cast<int>((K + gws::BK - 1) / gws::BK);
-  p.group_m = 16;
+  p.group_m = h->group_m;
+  p.staging_tiles_m = static_cast<int>((M + gws::STAGING - 1) / gws::STAGING);
   p.staging_tiles_n = static_cast<int>(stn);
   p.alpha = alpha;
   p.beta = beta;
@@ -137,11 +171,46 @@ int launch(gemm_ws* h, const uint16_t* A, const uint16_t* B, const uint16_t* C, 
     if (e == cudaSuccess) e = cudaMemsetAsync(h->work, 0, sizeof(uint32_t), stream);
     if (e != cudaSuccess) return cuda_fail(h, e);
   }
-  const int grid = static_cast<int>(num_tiles < h->num_sms ? num_tiles : h->num_sms);
-  gws::gemm_ws_kernel<<<grid, gws::NUM_THREADS, gws::SMEM_BYTES, stream>>>(p);
-  e = cudaGetLastError();
+  if (cg == 1) {
+    const int grid = static_cast<int>(num_tiles < h->num_sms ? num_tiles : h->num_sms);
+    gws::gemm_ws_kernel<1><<<grid, gws::NUM_THREADS, gws::Cfg<1>::SMEM_BYTES, stream>>>(p);
+    e = cudaGetLastError();
+  } else {
+    const int64_t clusters = num_tiles < h->max_pair_clusters ? num_tiles : h->max_pair_clusters;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(static_cast<unsigned>(2 * clusters), 1, 1);
+    cfg.blockDim = dim3(gws::NUM_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = gws::Cfg<2>::SMEM_BYTES;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, gws::gemm_ws_kernel<2>, p);
+  }
   if (e != cudaSuccess) return cuda_fail(h, e);
   return GEMM_WS_OK;
+}
+
+// GEMM_WS_CTA_GROUP=1 selects single-CTA 128 x 256 tiles; the default is
+// CTA-pair 256 x 256 tiles.
+int cta_group_from_env() {
+  if (const char* s = std::getenv("GEMM_WS_CTA_GROUP")) {
+    if (std::atoi(s) == 1) return 1;
+  }
+  return 2;
+}
+
+// GEMM_WS_GROUP_M overrides the raster group (m-tiles per n step; default 8).
+int group_m_from_env() {
+  if (const char* s = std::getenv("GEMM_WS_GROUP_M")) {
+    const int g = std::atoi(s);
+    if (g >= 1 && g <= 1024) return g;
+  }
+  return 8;
 }
 
 class DeviceGuard {
@@ -196,8 +265,10 @@ int gemm_ws_create(gemm_ws_t** out, int device) {
   }
   h->encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
 
-  e = cudaFuncSetAttribute(gws::gemm_ws_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(gws::SMEM_BYTES));
+  h->cta_group = cta_group_from_env();
+  h->group_m = group_m_from_env();
+  e = configure_kernels(h->num_sms, &h->max_pair_clusters);
+  if (e == cudaSuccess && h->max_pair_clusters < 1) h->cta_group = 1;
   if (e == cudaSuccess) e = cudaMalloc(&h->work, 2 * sizeof(uint32_t));
   if (e == cudaSuccess) e = cudaMemset(h->work, 0, 2 * sizeof(uint32_t));
   if (e != cudaSuccess) {
@@ -310,6 +381,8 @@ constexpr int kNoAllocMaxDevices = 64;
 struct NoAllocDevice {
   bool ready;
   int num_sms;
+  int cta_group;
+  int max_pair_clusters;
   uint32_t* scratch;   // device address of g_noalloc_scratch on this device
   unsigned long long timeout_ns;
   PFN_cuTensorMapEncodeTiled_v12000 encode;
@@ -345,9 +418,10 @@ int noalloc_setup(int device, NoAllocDevice** out) {
                                          &q) != cudaSuccess ||
         q != cudaDriverEntryPointSuccess || !fn)
       return GEMM_WS_ERR_CUDA;
-    if (cudaFuncSetAttribute(gws::gemm_ws_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(gws::SMEM_BYTES)) != cudaSuccess)
-      return GEMM_WS_ERR_CUDA;
+    int pair_clusters = 0;
+    if (configure_kernels(sms, &pair_clusters) != cudaSuccess) return GEMM_WS_ERR_CUDA;
+    d.cta_group = pair_clusters >= 1 ? cta_group_from_env() : 1;
+    d.max_pair_clusters = pair_clusters;
     uint32_t* ptr = nullptr;
     // In host code the array's name is only a host-side stand-in; the kernel
     // must be given this device address instead.
@@ -387,6 +461,9 @@ extern "C" int gemm_ws_run_streamout_noalloc(const uint16_t* A, const uint16_t* 
   std::memset(&h, 0, sizeof h);
   h.device = device;
   h.num_sms = d->num_sms;
+  h.cta_group = d->cta_group;
+  h.group_m = group_m_from_env();
+  h.max_pair_clusters = d->max_pair_clusters;
   h.work = d->scratch;
   h.timeout_ns = d->timeout_ns;
   h.encode = d->encode;

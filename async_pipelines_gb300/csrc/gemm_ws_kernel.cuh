@@ -10,7 +10,7 @@
 //              mainloop `load()` discussed in "why does load() pre-issue
 //              producer_try_acquire", it probes the NEXT stage's empty barrier
 //              (non-blocking token) before issuing the current stage's copies.
-//   warp 1     MMA issuer: one thread issues tcgen05.mma (128 x 256 x 16)
+//   warp 1     MMA issuer: one thread issues tcgen05.mma (N = 256, K = 16)
 //              into one of two TMEM accumulators and releases each stage with
 //              tcgen05.commit -> empty[s]; a tile's last commit -> acc_full.
 //   warps 2-5  epilogue: each warp owns one 32-lane quarter of TMEM (rows),
@@ -29,8 +29,24 @@
 //              d_empty, which is the answer to the issue's problem that bulk
 //              groups are per thread and invisible to another warp.
 //
-// Every role walks the same static persistent tile sequence (tile
-// blockIdx.x, then + gridDim.x, ...), so the scheduler needs no communication.
+// CTA group CG (template parameter):
+//   CG == 1  one CTA computes a 128 x 256 tile (tcgen05.mma.cta_group::1,
+//            M = 128); it loads a 128 x 64 slab of A and a 256 x 64 slab of B
+//            per k-block.
+//   CG == 2  a cluster of two CTAs computes a 256 x 256 tile with
+//            tcgen05.mma.cta_group::2 (M = 256) issued by the even CTA only;
+//            each CTA loads its own 128 rows of A and its own 128 rows of B
+//            (128 x 64 each, no multicast), and each CTA's TMEM receives its
+//            128 rows of D. The TMA of both CTAs completes on the even CTA's
+//            full[s] barrier, which the even producer arms for both; the MMA's
+//            commits are multicast to both CTAs' empty / acc_full barriers;
+//            the epilogue warps of both CTAs release acc_empty on the even
+//            CTA. This is the CTA-pair pipeline of the CuTe DSL pipeline page
+//            (UMMA commits per CTA group, async producers signalling the even
+//            CTA of the pair).
+//
+// Every role walks the same static persistent tile sequence (cluster c takes
+// tiles c, c + #clusters, ...), so the scheduler needs no communication.
 // Every wait is bounded by a watchdog (global timer): on expiry the kernel
 // records GEMM_WS_ERR_TIMEOUT in a status word, all roles leave their loops,
 // in-flight copies are drained and TMEM is freed.
@@ -43,14 +59,12 @@
 
 namespace gws {
 
-constexpr int BM = 128;                  // tile rows   (UMMA M)
-constexpr int BN = 256;                  // tile cols   (UMMA N)
+constexpr int BM = 128;                  // rows per CTA = TMEM lanes
+constexpr int BN = 256;                  // tile columns (UMMA N)
 constexpr int BK = 64;                   // k-block: 64 bf16 = one 128-byte swizzle row
 constexpr int UMMA_K = 16;               // K of one tcgen05.mma kind::f16
-constexpr int STAGES = 4;                // mainloop ring depth
 constexpr int ACC_BUFS = 2;              // TMEM accumulators (MMA overlaps epilogue)
 constexpr int EPI_N = 32;                // columns per epilogue subtile
-constexpr int EPI_SUB = BN / EPI_N;      // subtiles per tile
 constexpr int EPI_SLOTS = 2;             // D shared-memory slots (store pipeline depth)
 constexpr int C_BUFS = 2;                // C shared-memory buffers per epilogue warp
 constexpr int NUM_EPI_WARPS = 4;
@@ -62,47 +76,58 @@ constexpr int WARP_EPI0 = 2;
 constexpr int WARP_CONSUMER = 6;
 constexpr int NUM_THREADS = 7 * 32;
 constexpr uint32_t TMEM_COLS = ACC_BUFS * BN;   // 512: all of the SM's TMEM
-
 constexpr uint32_t A_STAGE_BYTES = BM * BK * 2;          // 16 KiB
-constexpr uint32_t B_STAGE_BYTES = BN * BK * 2;          // 32 KiB
-constexpr uint32_t STAGE_TX_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
 constexpr uint32_t EPI_QUARTER_BYTES = 32 * EPI_N * 2;   // 2 KiB: one warp's rows
 constexpr uint32_t EPI_SLOT_BYTES = BM * EPI_N * 2;      // 8 KiB: 128 rows
+constexpr uint32_t STATUS_TIMEOUT = 5;   // == GEMM_WS_ERR_TIMEOUT
+constexpr uint32_t WAIT_HINT_NS = 1000000;   // suspend bound of one try_wait
 
-// Shared-memory carve-out (offsets from a 1024-byte aligned base).
-constexpr uint32_t OFF_A = 0;
-constexpr uint32_t OFF_B = OFF_A + STAGES * A_STAGE_BYTES;
-constexpr uint32_t OFF_D = OFF_B + STAGES * B_STAGE_BYTES;
-constexpr uint32_t OFF_C = OFF_D + EPI_SLOTS * EPI_SLOT_BYTES;
-constexpr uint32_t OFF_BAR = OFF_C + C_BUFS * EPI_SLOT_BYTES;
 // barrier indices
+constexpr int NUM_STAGES_MAX = 6;
 constexpr int BAR_FULL = 0;
-constexpr int BAR_EMPTY = BAR_FULL + STAGES;
-constexpr int BAR_ACC_FULL = BAR_EMPTY + STAGES;
+constexpr int BAR_EMPTY = BAR_FULL + NUM_STAGES_MAX;
+constexpr int BAR_ACC_FULL = BAR_EMPTY + NUM_STAGES_MAX;
 constexpr int BAR_ACC_EMPTY = BAR_ACC_FULL + ACC_BUFS;
 constexpr int BAR_C_FULL = BAR_ACC_EMPTY + ACC_BUFS;          // [warp quarter][buf]
 constexpr int BAR_D_FULL = BAR_C_FULL + NUM_EPI_WARPS * C_BUFS;
 constexpr int BAR_D_EMPTY = BAR_D_FULL + EPI_SLOTS;
 constexpr int BAR_MMA_DRAIN = BAR_D_EMPTY + EPI_SLOTS;
 constexpr int NUM_BARS = BAR_MMA_DRAIN + 1;
-constexpr uint32_t OFF_TMEM_SLOT = OFF_BAR + NUM_BARS * 8;
-constexpr uint32_t OFF_ABORT = OFF_TMEM_SLOT + 4;
-constexpr uint32_t SMEM_USED = OFF_ABORT + 4;
-constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;   // + slack to align the base
-static_assert(SMEM_BYTES <= 232448, "exceeds the 227 KiB per-CTA shared memory");
-static_assert(OFF_B % 1024 == 0 && OFF_D % 1024 == 0 && OFF_C % 1024 == 0, "alignment");
 
-constexpr uint32_t STATUS_TIMEOUT = 5;   // == GEMM_WS_ERR_TIMEOUT
+template <int CG>
+struct Cfg {
+  static_assert(CG == 1 || CG == 2, "CTA group of 1 or 2");
+  static constexpr int TILE_M = BM * CG;                 // rows per (pair) tile
+  static constexpr int B_ROWS = BN / CG;                 // B rows each CTA loads
+  static constexpr int STAGES = CG == 1 ? 4 : 6;
+  static constexpr uint32_t B_STAGE_BYTES = B_ROWS * BK * 2;
+  static constexpr uint32_t STAGE_TX = CG * (A_STAGE_BYTES + B_STAGE_BYTES);
+  // Shared-memory carve-out (offsets from a 1024-byte aligned base).
+  static constexpr uint32_t OFF_A = 0;
+  static constexpr uint32_t OFF_B = OFF_A + STAGES * A_STAGE_BYTES;
+  static constexpr uint32_t OFF_D = OFF_B + STAGES * B_STAGE_BYTES;
+  static constexpr uint32_t OFF_C = OFF_D + EPI_SLOTS * EPI_SLOT_BYTES;
+  static constexpr uint32_t OFF_BAR = OFF_C + C_BUFS * EPI_SLOT_BYTES;
+  static constexpr uint32_t OFF_TMEM_SLOT = OFF_BAR + NUM_BARS * 8;
+  static constexpr uint32_t OFF_ABORT = OFF_TMEM_SLOT + 4;
+  static constexpr uint32_t SMEM_USED = OFF_ABORT + 4;
+  static constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;   // + slack to align the base
+  static constexpr uint32_t IDESC = idesc_bf16_f32(TILE_M, BN);
+  static_assert(STAGES <= NUM_STAGES_MAX, "barrier table");
+  static_assert(SMEM_BYTES <= 232448, "exceeds the 227 KiB per-CTA shared memory");
+  static_assert(OFF_B % 1024 == 0 && OFF_D % 1024 == 0 && OFF_C % 1024 == 0, "alignment");
+};
 
 struct Params {
   CUtensorMap tmA;   // {K, M, L}, box {64, 128}, 128-byte swizzle
-  CUtensorMap tmB;   // {K, N, L}, box {64, 256}, 128-byte swizzle
+  CUtensorMap tmB;   // {K, N, L}, box {64, 256 / CG}, 128-byte swizzle
   CUtensorMap tmC;   // {N, M, L}, box {32, 32},  64-byte swizzle (beta != 0)
   CUtensorMap tmD;   // {N, M, L}, box {32, 32},  64-byte swizzle
   CUtensorMap tmS;   // staging {128, 128, T}, box {32, 128}, 64-byte swizzle
   int M, N, K, L;
-  int tiles_m, tiles_n, num_tiles, num_kb;
+  int tiles_m, tiles_n, num_tiles, num_kb;   // tiles of 128*CG x 256
   int group_m;                   // raster: tiles walk group_m m-tiles per n step
+  int staging_tiles_m;           // ceil(M / 128)
   int staging_tiles_n;           // ceil(N / 128)
   float alpha, beta;
   int has_c;                     // beta != 0
@@ -129,8 +154,10 @@ __device__ __forceinline__ void tile_coords(const Params& p, int t, int& mb, int
   nb = rr / gm;
 }
 
-// Stream-out tiles (128 columns) of output tile `nb` that exist: 1 or 2.
-__device__ __forceinline__ int staging_in_tile(const Params& p, int nb) {
+// Stream-out tiles (128 x 128) of this CTA's 128 x 256 part of a tile that
+// exist inside M x N: 0, 1 or 2. Epilogue and consumer use the same count.
+__device__ __forceinline__ int staging_in_part(const Params& p, int row_tile, int nb) {
+  if (row_tile >= p.staging_tiles_m) return 0;
   const int cols_left = p.N - nb * BN;
   return min(BN / STAGING, (cols_left + STAGING - 1) / STAGING);
 }
@@ -141,20 +168,42 @@ struct Watchdog {
   unsigned long long limit_ns;
 };
 
-// Bounded wait on an mbarrier phase. Returns false if the CTA is aborting or
-// this wait exceeded the limit (which then starts the abort).
+// Bounded wait on an mbarrier phase. The probe may suspend the thread until
+// the phase completes (or WAIT_HINT_NS passes), so waiting costs few issue
+// slots. Returns false if the CTA is aborting or this wait exceeded the limit
+// (which then starts the abort). kCluster selects cluster-scope acquire, for
+// barriers that the peer CTA arrives on.
+template <bool kCluster>
 __device__ __noinline__ bool wait_bounded(uint32_t bar, uint32_t parity, const Watchdog& wd) {
-  if (mbar_try_wait(bar, parity)) return true;
+  auto probe = [&]() {
+    uint32_t ok;
+    if (kCluster)
+      asm volatile(
+          "{\n\t.reg .pred p;\n\t"
+          "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
+          "selp.u32 %0, 1, 0, p;\n\t}"
+          : "=r"(ok)
+          : "r"(bar), "r"(parity), "r"(WAIT_HINT_NS)
+          : "memory");
+    else
+      asm volatile(
+          "{\n\t.reg .pred p;\n\t"
+          "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+          "selp.u32 %0, 1, 0, p;\n\t}"
+          : "=r"(ok)
+          : "r"(bar), "r"(parity), "r"(WAIT_HINT_NS)
+          : "memory");
+    return ok != 0;
+  };
+  if (probe()) return true;
   const uint64_t t0 = global_timer_ns();
-  for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 7) == 0) {
-      if (*wd.abort) return false;
-      if (global_timer_ns() - t0 > wd.limit_ns) {
-        *wd.abort = 1;
-        atomicExch(wd.status, STATUS_TIMEOUT);
-        return false;
-      }
+  for (;;) {
+    if (probe()) return true;
+    if (*wd.abort) return false;
+    if (global_timer_ns() - t0 > wd.limit_ns) {
+      *wd.abort = 1;
+      atomicExch(wd.status, STATUS_TIMEOUT);
+      return false;
     }
   }
 }
@@ -162,7 +211,7 @@ __device__ __noinline__ bool wait_bounded(uint32_t bar, uint32_t parity, const W
 // Short bounded wait used only while draining after an abort.
 __device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity) {
   const uint64_t t0 = global_timer_ns();
-  while (!mbar_try_wait(bar, parity)) {
+  while (!mbar_try_wait_cluster(bar, parity)) {
     if (global_timer_ns() - t0 > 100000000ull) return;   // 100 ms
   }
 }
@@ -174,93 +223,128 @@ __device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity) {
 // needs an arrival that this warp makes only later.
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const Watchdog& wd) {
   uint32_t ok = 0;
-  if ((threadIdx.x & 31) == 0) ok = wait_bounded(bar, parity, wd) ? 1u : 0u;
+  if ((threadIdx.x & 31) == 0) ok = wait_bounded<true>(bar, parity, wd) ? 1u : 0u;
   ok = __shfl_sync(0xffffffffu, ok, 0);
-  if (ok) (void)mbar_try_wait(bar, parity);
+  if (ok) (void)mbar_try_wait_cluster(bar, parity);
   __syncwarp();
   return ok != 0;
 }
 
 // ------------------------------------------------------------ producer
 
-__device__ __forceinline__ void producer_role(const Params& p, uint32_t sbase,
+template <int CG>
+__device__ __forceinline__ void producer_role(const Params& p, uint32_t sbase, uint32_t rank,
                                               const Watchdog& wd) {
-  auto full = [&](uint32_t s) { return sbase + OFF_BAR + 8 * (BAR_FULL + s); };
-  auto empty = [&](uint32_t s) { return sbase + OFF_BAR + 8 * (BAR_EMPTY + s); };
+  using C = Cfg<CG>;
+  auto full = [&](uint32_t s) { return sbase + C::OFF_BAR + 8 * (BAR_FULL + s); };
+  auto empty = [&](uint32_t s) { return sbase + C::OFF_BAR + 8 * (BAR_EMPTY + s); };
+  const int cluster = blockIdx.x / CG, clusters = gridDim.x / CG;
   uint32_t g = 0;   // k-blocks issued by this CTA so far (ring position)
   bool ok = true;
   // The producer starts in the opposite phase: the first STAGES waits on a
   // freshly initialised empty barrier (parity 1) succeed at once.
   bool token = mbar_test_wait(empty(0), 1);
-  for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+  for (int t = cluster; ok && t < p.num_tiles; t += clusters) {
     int mb, nb, l;
     tile_coords(p, t, mb, nb, l);
-    const int m0 = mb * BM, n0 = nb * BN;
+    const int a_row = mb * C::TILE_M + static_cast<int>(rank) * BM;
+    const int b_row = nb * BN + static_cast<int>(rank) * C::B_ROWS;
     for (int kb = 0; kb < p.num_kb; ++kb) {
-      const uint32_t s = g % STAGES;
-      const uint32_t ph = (g / STAGES) & 1;
-      if (!token && !wait_bounded(empty(s), ph ^ 1, wd)) {
+      const uint32_t s = g % C::STAGES;
+      const uint32_t ph = (g / C::STAGES) & 1;
+      if (!token && !wait_bounded<false>(empty(s), ph ^ 1, wd)) {
         ok = false;
         break;
       }
       ++g;
       // try-acquire the NEXT stage before this stage's copies go out
-      token = mbar_test_wait(empty(g % STAGES), ((g / STAGES) & 1) ^ 1);
-      mbar_arrive_expect_tx(full(s), STAGE_TX_BYTES);
-      tma_load_3d(sbase + OFF_A + s * A_STAGE_BYTES, &p.tmA, full(s), kb * BK, m0, l);
-      tma_load_3d(sbase + OFF_B + s * B_STAGE_BYTES, &p.tmB, full(s), kb * BK, n0, l);
+      token = mbar_test_wait(empty(g % C::STAGES), ((g / C::STAGES) & 1) ^ 1);
+      if constexpr (CG == 1) {
+        mbar_arrive_expect_tx(full(s), C::STAGE_TX);
+        tma_load_3d(sbase + C::OFF_A + s * A_STAGE_BYTES, &p.tmA, full(s), kb * BK, a_row, l);
+        tma_load_3d(sbase + C::OFF_B + s * C::B_STAGE_BYTES, &p.tmB, full(s), kb * BK, b_row, l);
+      } else {
+        // Both CTAs' copies complete on the even CTA's full[s]; it arms the
+        // barrier for the bytes of both.
+        if (rank == 0) mbar_arrive_expect_tx(full(s), C::STAGE_TX);
+        const uint32_t leader_full = mapa_shared(full(s), 0);
+        tma_load_3d_pair(sbase + C::OFF_A + s * A_STAGE_BYTES, &p.tmA, leader_full, kb * BK,
+                         a_row, l);
+        tma_load_3d_pair(sbase + C::OFF_B + s * C::B_STAGE_BYTES, &p.tmB, leader_full, kb * BK,
+                         b_row, l);
+      }
     }
   }
-  if (!ok) {
+  if (!ok && rank == 0) {
     // Abort: wait (bounded) for the copies of the last stages issued, so no
-    // TMA write lands after the CTA has released its shared memory.
-    const uint32_t first = g > STAGES ? g - STAGES : 0;
-    for (uint32_t j = first; j < g; ++j) wait_drain(full(j % STAGES), (j / STAGES) & 1);
+    // TMA write lands after the CTA pair has released its shared memory.
+    const uint32_t first = g > C::STAGES ? g - C::STAGES : 0;
+    for (uint32_t j = first; j < g; ++j) wait_drain(full(j % C::STAGES), (j / C::STAGES) & 1);
   }
 }
 
 // ------------------------------------------------------------ MMA issuer
 
+template <int CG>
 __device__ __forceinline__ void mma_role(const Params& p, uint32_t sbase, uint32_t tmem_base,
                                          const Watchdog& wd) {
-  auto bar = [&](int i) { return sbase + OFF_BAR + 8 * i; };
-  constexpr uint32_t idesc = idesc_bf16_f32(BM, BN);
+  using C = Cfg<CG>;
+  auto bar = [&](int i) { return sbase + C::OFF_BAR + 8 * i; };
+  auto commit = [&](uint32_t b) {
+    if constexpr (CG == 1)
+      umma_commit(b);
+    else
+      umma_commit_pair(b, 0x3);
+  };
+  const int cluster = blockIdx.x / CG, clusters = gridDim.x / CG;
   uint32_t g = 0;
   int i = 0;
   bool issued = false;
-  for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++i) {
+  for (int t = cluster; t < p.num_tiles; t += clusters, ++i) {
     const uint32_t b = i & 1, aph = (i >> 1) & 1;
-    if (!wait_bounded(bar(BAR_ACC_EMPTY + b), aph ^ 1, wd)) goto done;
+    if (!wait_bounded<true>(bar(BAR_ACC_EMPTY + b), aph ^ 1, wd)) goto done;
     tc_fence_after_sync();
     {
       const uint32_t d_tmem = tmem_base + b * BN;
       for (int kb = 0; kb < p.num_kb; ++kb) {
-        const uint32_t s = g % STAGES;
-        if (!wait_bounded(bar(BAR_FULL + s), (g / STAGES) & 1, wd)) goto done;
+        const uint32_t s = g % C::STAGES;
+        if (!wait_bounded<true>(bar(BAR_FULL + s), (g / C::STAGES) & 1, wd)) goto done;
         tc_fence_after_sync();
-        const uint32_t a_addr = sbase + OFF_A + s * A_STAGE_BYTES;
-        const uint32_t b_addr = sbase + OFF_B + s * B_STAGE_BYTES;
+        const uint32_t a_addr = sbase + C::OFF_A + s * A_STAGE_BYTES;
+        const uint32_t b_addr = sbase + C::OFF_B + s * C::B_STAGE_BYTES;
 #pragma unroll
         for (int kk = 0; kk < BK / UMMA_K; ++kk) {
-          umma_bf16(d_tmem, sdesc_kmajor_sw128(a_addr + kk * UMMA_K * 2),
-                    sdesc_kmajor_sw128(b_addr + kk * UMMA_K * 2), idesc,
-                    (kb | kk) != 0 ? 1u : 0u);
+          const uint64_t ad = sdesc_kmajor_sw128(a_addr + kk * UMMA_K * 2);
+          const uint64_t bd = sdesc_kmajor_sw128(b_addr + kk * UMMA_K * 2);
+          const uint32_t acc = (kb | kk) != 0 ? 1u : 0u;
+          if constexpr (CG == 1)
+            umma_bf16(d_tmem, ad, bd, C::IDESC, acc);
+          else
+            umma_bf16_pair(d_tmem, ad, bd, C::IDESC, acc);
         }
         issued = true;
-        umma_commit(bar(BAR_EMPTY + s));   // stage s free once these MMAs finish
+        commit(bar(BAR_EMPTY + s));   // stage s free (in every CTA) once these finish
         ++g;
       }
     }
-    if (p.num_kb > 0)
-      umma_commit(bar(BAR_ACC_FULL + b));   // accumulator b complete
-    else
-      mbar_arrive(bar(BAR_ACC_FULL + b));   // K == 0: nothing to wait for
+    if (p.num_kb > 0) {
+      commit(bar(BAR_ACC_FULL + b));   // accumulator b complete (in every CTA)
+    } else {
+      // K == 0: no MMA ran; signal the accumulator barriers directly.
+      if constexpr (CG == 1)
+        mbar_arrive(bar(BAR_ACC_FULL + b));
+      else
+        for (int r = 0; r < CG; ++r) mbar_arrive_cluster(mapa_shared(bar(BAR_ACC_FULL + b), r));
+    }
   }
 done:
   if (issued) {
     // Every MMA this thread issued has finished once this arrives; TMEM can
     // then be freed even on the abort path.
-    umma_commit(bar(BAR_MMA_DRAIN));
+    if constexpr (CG == 1)
+      umma_commit(bar(BAR_MMA_DRAIN));
+    else
+      umma_commit_pair(bar(BAR_MMA_DRAIN), 0x1);
     wait_drain(bar(BAR_MMA_DRAIN), 0);
   }
 }
@@ -281,24 +365,29 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
+template <int CG>
 __device__ __forceinline__ void epilogue_role(const Params& p, uint32_t sbase, uint8_t* smem,
-                                              uint32_t tmem_base, int warp, const Watchdog& wd) {
+                                              uint32_t tmem_base, uint32_t rank, int warp,
+                                              const Watchdog& wd) {
+  using C = Cfg<CG>;
   const int lane = threadIdx.x & 31;
-  const int q = warp & 3;   // TMEM lane quarter this warp may access = tile rows 32q..32q+31
-  auto bar = [&](int i) { return sbase + OFF_BAR + 8 * i; };
+  const int q = warp & 3;   // TMEM lane quarter this warp may access = CTA rows 32q..32q+31
+  auto bar = [&](int i) { return sbase + C::OFF_BAR + 8 * i; };
   // 64-byte swizzle of a 32-row x 64-byte block: 16-byte chunk c of row r is
   // stored at chunk c ^ ((r >> 1) & 3); the same pattern TMA uses.
   const uint32_t row_off = lane * 64;
   const uint32_t swz = (lane >> 1) & 3;
+  const int cluster = blockIdx.x / CG, clusters = gridDim.x / CG;
   uint32_t u = 0;        // subtiles stored by this warp (D slot ring position)
   uint32_t cu = 0;       // C subtiles consumed by this warp (C ring position)
   uint32_t c_issued = 0; // C subtile loads issued by this warp
   int i = 0;
-  for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++i) {
+  for (int t = cluster; t < p.num_tiles; t += clusters, ++i) {
     int mb, nb, l;
     tile_coords(p, t, mb, nb, l);
-    const int m0 = mb * BM + 32 * q, n0 = nb * BN;
-    const int nsub = staging_in_tile(p, nb) * SUB_PER_STAGING;
+    const int row_tile = mb * CG + static_cast<int>(rank);   // this CTA's 128-row slab
+    const int m0 = row_tile * BM + 32 * q, n0 = nb * BN;
+    const int nsub = staging_in_part(p, row_tile, nb) * SUB_PER_STAGING;
     const uint32_t b = i & 1, aph = (i >> 1) & 1;
 
     auto issue_c = [&](int j) {
@@ -308,15 +397,27 @@ __device__ __forceinline__ void epilogue_role(const Params& p, uint32_t sbase, u
         const uint32_t cbar = bar(BAR_C_FULL + q * C_BUFS + cb);
         fence_proxy_async_smem();   // earlier generic reads of this buffer come first
         mbar_arrive_expect_tx(cbar, EPI_QUARTER_BYTES);
-        tma_load_3d(sbase + OFF_C + cb * EPI_SLOT_BYTES + q * EPI_QUARTER_BYTES, &p.tmC, cbar,
+        tma_load_3d(sbase + C::OFF_C + cb * EPI_SLOT_BYTES + q * EPI_QUARTER_BYTES, &p.tmC, cbar,
                     n0 + j * EPI_N, m0, l);
       }
     };
-    if (p.has_c) issue_c(0);
+    auto release_acc = [&]() {
+      // Accumulator b fully read: hand it back to the MMA warp (even CTA).
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) {
+        if constexpr (CG == 1)
+          mbar_arrive(bar(BAR_ACC_EMPTY + b));
+        else
+          mbar_arrive_cluster(mapa_shared(bar(BAR_ACC_EMPTY + b), 0));
+      }
+    };
+    if (p.has_c && nsub > 0) issue_c(0);
 
     if (!warp_wait(bar(BAR_ACC_FULL + b), aph, wd)) break;
     tc_fence_after_sync();
     const uint32_t tacc = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + b * BN;
+    if (nsub == 0) release_acc();   // this CTA's rows lie outside M
 
     bool ok = true;
     for (int j = 0; j < nsub; ++j) {
@@ -330,12 +431,7 @@ __device__ __forceinline__ void epilogue_role(const Params& p, uint32_t sbase, u
 #pragma unroll
         for (int e = 0; e < 32; ++e) acc[e] = 0u;
       }
-      if (j == nsub - 1) {
-        // Accumulator b fully read: hand it back to the MMA warp.
-        tc_fence_before_sync();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(BAR_ACC_EMPTY + b));
-      }
+      if (j == nsub - 1) release_acc();
 
       float v[32];
 #pragma unroll
@@ -346,7 +442,8 @@ __device__ __forceinline__ void epilogue_role(const Params& p, uint32_t sbase, u
           ok = false;
           break;
         }
-        const uint8_t* cbase = smem + OFF_C + cb * EPI_SLOT_BYTES + q * EPI_QUARTER_BYTES + row_off;
+        const uint8_t* cbase =
+            smem + C::OFF_C + cb * EPI_SLOT_BYTES + q * EPI_QUARTER_BYTES + row_off;
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           const uint4 raw = *reinterpret_cast<const uint4*>(cbase + ((c ^ swz) << 4));
@@ -369,7 +466,7 @@ __device__ __forceinline__ void epilogue_role(const Params& p, uint32_t sbase, u
         }
       }
       __syncwarp();
-      uint8_t* dq = smem + OFF_D + slot * EPI_SLOT_BYTES + q * EPI_QUARTER_BYTES;
+      uint8_t* dq = smem + C::OFF_D + slot * EPI_SLOT_BYTES + q * EPI_QUARTER_BYTES;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint4 w;
@@ -401,22 +498,27 @@ __device__ __forceinline__ void epilogue_role(const Params& p, uint32_t sbase, u
 
 // ------------------------------------------------------------ stream-out consumer
 
-__device__ __forceinline__ void consumer_role(const Params& p, uint32_t sbase,
+template <int CG>
+__device__ __forceinline__ void consumer_role(const Params& p, uint32_t sbase, uint32_t rank,
                                               const Watchdog& wd) {
-  auto bar = [&](int i) { return sbase + OFF_BAR + 8 * i; };
+  using C = Cfg<CG>;
+  auto bar = [&](int i) { return sbase + C::OFF_BAR + 8 * i; };
+  const int cluster = blockIdx.x / CG, clusters = gridDim.x / CG;
   uint32_t u = 0;
-  for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
+  for (int t = cluster; t < p.num_tiles; t += clusters) {
     int mb, nb, l;
     tile_coords(p, t, mb, nb, l);
-    const int nst = staging_in_tile(p, nb);
+    const int row_tile = mb * CG + static_cast<int>(rank);
+    const int nst = staging_in_part(p, row_tile, nb);
     for (int st = 0; st < nst; ++st) {
-      const int tile_id = (l * p.tiles_m + mb) * p.staging_tiles_n + nb * (BN / STAGING) + st;
+      const int tile_id =
+          (l * p.staging_tiles_m + row_tile) * p.staging_tiles_n + nb * (BN / STAGING) + st;
       uint32_t seq = 0;
       for (int jj = 0; jj < SUB_PER_STAGING; ++jj) {
         const uint32_t slot = u % EPI_SLOTS;
-        if (!wait_bounded(bar(BAR_D_FULL + slot), (u / EPI_SLOTS) & 1, wd)) goto done;
+        if (!wait_bounded<false>(bar(BAR_D_FULL + slot), (u / EPI_SLOTS) & 1, wd)) goto done;
         if (jj == 0) seq = atomicAdd(p.counter, 1u);   // completion order
-        tma_store_3d(&p.tmS, sbase + OFF_D + slot * EPI_SLOT_BYTES, jj * EPI_N, 0,
+        tma_store_3d(&p.tmS, sbase + C::OFF_D + slot * EPI_SLOT_BYTES, jj * EPI_N, 0,
                      static_cast<int>(seq));
         bulk_commit();
         bulk_wait_read<0>();                  // slot read: give it back
@@ -436,7 +538,9 @@ done:
 
 // ------------------------------------------------------------ kernel
 
+template <int CG>
 __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_ws_kernel(const __grid_constant__ Params p) {
+  using C = Cfg<CG>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
   const uint32_t pad = ((raw + 1023u) & ~1023u) - raw;
@@ -444,18 +548,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_ws_kernel(const __grid_co
   const uint32_t sbase = raw + pad;
   const int warp = __shfl_sync(0xffffffffu, static_cast<int>(threadIdx.x / 32), 0);
   const int lane = threadIdx.x & 31;
-  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + OFF_ABORT);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_TMEM_SLOT);
+  const uint32_t rank = CG == 1 ? 0u : cluster_ctarank();
+  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + C::OFF_ABORT);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_TMEM_SLOT);
 
   if (warp == WARP_TMA && lane == 0) {
-    auto bar = [&](int i) { return sbase + OFF_BAR + 8 * i; };
-    for (int s = 0; s < STAGES; ++s) {
+    auto bar = [&](int i) { return sbase + C::OFF_BAR + 8 * i; };
+    for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(bar(BAR_FULL + s), 1);
       mbar_init(bar(BAR_EMPTY + s), 1);
     }
     for (int b = 0; b < ACC_BUFS; ++b) {
       mbar_init(bar(BAR_ACC_FULL + b), 1);
-      mbar_init(bar(BAR_ACC_EMPTY + b), NUM_EPI_WARPS);
+      mbar_init(bar(BAR_ACC_EMPTY + b), NUM_EPI_WARPS * CG);
     }
     for (int i = 0; i < NUM_EPI_WARPS * C_BUFS; ++i) mbar_init(bar(BAR_C_FULL + i), 1);
     for (int s = 0; s < EPI_SLOTS; ++s) {
@@ -474,31 +579,43 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_ws_kernel(const __grid_co
     if (p.streamout) prefetch_tensormap(&p.tmS);
   }
   if (warp == WARP_MMA) {
-    tmem_alloc(smem_addr(tmem_slot), TMEM_COLS);
-    tmem_relinquish();
+    if constexpr (CG == 1) {
+      tmem_alloc(smem_addr(tmem_slot), TMEM_COLS);
+      tmem_relinquish();
+    } else {
+      tmem_alloc_pair(smem_addr(tmem_slot), TMEM_COLS);
+      tmem_relinquish_pair();
+    }
   }
   tc_fence_before_sync();
   __syncthreads();
+  if constexpr (CG == 2) cluster_sync();   // peer's barriers initialised before any remote use
   tc_fence_after_sync();
   const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
   const Watchdog wd{abort_flag, p.status, p.timeout_ns};
 
   if (warp == WARP_TMA) {
-    if (lane == 0) producer_role(p, sbase, wd);
+    if (lane == 0) producer_role<CG>(p, sbase, rank, wd);
   } else if (warp == WARP_MMA) {
-    if (lane == 0) mma_role(p, sbase, tmem_base, wd);
+    if (lane == 0 && rank == 0) mma_role<CG>(p, sbase, tmem_base, wd);
   } else if (warp < WARP_EPI0 + NUM_EPI_WARPS) {
-    epilogue_role(p, sbase, smem, tmem_base, warp, wd);
+    epilogue_role<CG>(p, sbase, smem, tmem_base, rank, warp, wd);
   } else if (warp == WARP_CONSUMER && p.streamout) {
-    if (lane == 0) consumer_role(p, sbase, wd);
+    if (lane == 0) consumer_role<CG>(p, sbase, rank, wd);
   }
 
   __syncwarp();
   tc_fence_before_sync();
   __syncthreads();
+  // The peer may still arrive on, or have the tensor core read, this CTA's
+  // shared memory until both CTAs are here.
+  if constexpr (CG == 2) cluster_sync();
   if (warp == WARP_MMA) {
     tc_fence_after_sync();
-    tmem_dealloc(tmem_base, TMEM_COLS);
+    if constexpr (CG == 1)
+      tmem_dealloc(tmem_base, TMEM_COLS);
+    else
+      tmem_dealloc_pair(tmem_base, TMEM_COLS);
   }
 }
 

@@ -6,6 +6,7 @@ result must equal the oracle rounded to bf16 bit for bit.
 """
 from __future__ import annotations
 
+import os
 import numpy as np
 import pytest
 import torch
@@ -22,6 +23,24 @@ pytestmark = pytest.mark.gpu
 @pytest.fixture(scope="module")
 def gw():
     g = gemm_ws.GemmWS(0)
+    yield g
+    assert g.query_status() == gemm_ws.OK
+    g.close()
+
+
+@pytest.fixture(scope="module", params=[2, 1], ids=["cta_pair", "cta_single"])
+def gw_each(request):
+    """A handle per tile configuration: CTA-pair 256x256 tiles (the default)
+    and single-CTA 128x256 tiles (selected at create time by the environment)."""
+    old = os.environ.get("GEMM_WS_CTA_GROUP")
+    os.environ["GEMM_WS_CTA_GROUP"] = str(request.param)
+    try:
+        g = gemm_ws.GemmWS(0)
+    finally:
+        if old is None:
+            del os.environ["GEMM_WS_CTA_GROUP"]
+        else:
+            os.environ["GEMM_WS_CTA_GROUP"] = old
     yield g
     assert g.query_status() == gemm_ws.OK
     g.close()
@@ -45,7 +64,7 @@ def run_case(gw, M, N, K, L, alpha, beta, ab=("uniform",), cd=None, seed=0, rows
 
 # ------------------------------------------------------------------ exact cases
 
-def test_handworked_fixture(gw):
+def test_handworked_fixture(gw_each):
     """The hand-worked 2x3x4 example, zero-padded to K = N = 8 (16-byte rows)."""
     A, Bkn, C, Dexp, alpha, beta = load_handworked()
     M, K = A.shape
@@ -56,7 +75,7 @@ def test_handworked_fixture(gw):
     t = lambda x: torch.from_numpy(f64_to_bf16_bits(x).astype(np.int16)).view(
         torch.bfloat16).reshape(1, *x.shape).cuda()
     D = torch.empty(1, M, 8, dtype=torch.bfloat16, device="cuda")
-    gw.run(t(Ap), t(Bp), t(Cp), D, alpha, beta)
+    gw_each.run(t(Ap), t(Bp), t(Cp), D, alpha, beta)
     torch.cuda.synchronize()
     got = bits_of(D).reshape(M, 8)
     np.testing.assert_array_equal(got[:, :N], f64_to_bf16_bits(Dexp))
@@ -69,10 +88,10 @@ def test_handworked_fixture(gw):
     (1, 8, 8, 1),           # smallest legal problem
     (2048, 2048, 128, 1),   # more tiles than SMs: persistent loop, ring wraps
 ])
-def test_integer_inputs_bit_exact(gw, M, N, K, L):
+def test_integer_inputs_bit_exact(gw_each, M, N, K, L):
     A, B, C = workloads.make_inputs(M, N, K, L, ("int", -4, 4), ("int", -4, 4), seed=M + K)
     D = torch.empty(L, M, N, dtype=torch.bfloat16, device="cuda")
-    gw.run(to_dev(A), to_dev(B), to_dev(C), D, 2.0, -3.0)
+    gw_each.run(to_dev(A), to_dev(B), to_dev(C), D, 2.0, -3.0)
     torch.cuda.synchronize()
     ref = oracle.gemm(bits_of(A), bits_of(B), bits_of(C), M, N, K, L, 2.0, -3.0)
     np.testing.assert_array_equal(bits_of(D).reshape(L, M, N), f64_to_bf16_bits(ref))
@@ -88,41 +107,41 @@ def test_integer_inputs_bit_exact(gw, M, N, K, L):
     (513, 1032, 1000, 1, 1.0, 1.0),
     (4096, 4096, 128, 1, 1.0, 0.0),   # 512 tiles: several tiles per CTA
 ])
-def test_small_shapes_match_oracle(gw, M, N, K, L, alpha, beta):
+def test_small_shapes_match_oracle(gw_each, M, N, K, L, alpha, beta):
     cd = ("normal", 1.0) if beta != 0 else None
-    d, ref = run_case(gw, M, N, K, L, alpha, beta, cd=cd, seed=17)
+    d, ref = run_case(gw_each, M, N, K, L, alpha, beta, cd=cd, seed=17)
     assert_gemm_close(d, ref, K, f"{M}x{N}x{K}x{L}")
 
 
-def test_k_zero_gives_beta_c(gw):
+def test_k_zero_gives_beta_c(gw_each):
     M, N, L = 200, 264, 2
     C = workloads.make_inputs(M, N, 0, L, ("uniform",), ("uniform",), 3)[2]
     D = torch.full((L, M, N), 7.0, dtype=torch.bfloat16, device="cuda")
     A = torch.empty(L, M, 0, dtype=torch.bfloat16, device="cuda")
     B = torch.empty(L, N, 0, dtype=torch.bfloat16, device="cuda")
-    gw.run(A, B, C.cuda(), D, 1.0, 0.5)
+    gw_each.run(A, B, C.cuda(), D, 1.0, 0.5)
     torch.cuda.synchronize()
     ref = oracle.gemm(np.zeros(0, np.uint16), np.zeros(0, np.uint16), bits_of(C),
                       M, N, 0, L, 1.0, 0.5)
     assert_gemm_close(bits_of(D), ref, 0, "K=0")
 
 
-def test_beta_zero_ignores_nan_c(gw):
+def test_beta_zero_ignores_nan_c(gw_each):
     M, N, K, L = 192, 256, 128, 1
     A, B, _ = workloads.make_inputs(M, N, K, L, ("uniform",), None, 5)
     C = torch.full((L, M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
     D = torch.empty(L, M, N, dtype=torch.bfloat16, device="cuda")
-    gw.run(A.cuda(), B.cuda(), C, D, 1.0, 0.0)
+    gw_each.run(A.cuda(), B.cuda(), C, D, 1.0, 0.0)
     torch.cuda.synchronize()
     ref = oracle.gemm(bits_of(A), bits_of(B), None, M, N, K, L, 1.0, 0.0)
     assert_gemm_close(bits_of(D), ref, K, "beta=0 with NaN C")
 
 
-def test_in_place_d_is_c(gw):
+def test_in_place_d_is_c(gw_each):
     M, N, K, L = 320, 392, 96, 2
     A, B, C = workloads.make_inputs(M, N, K, L, ("uniform",), ("normal", 1.0), 9)
     D = C.clone().cuda()
-    gw.run(A.cuda(), B.cuda(), D, D, 1.0, -1.0)
+    gw_each.run(A.cuda(), B.cuda(), D, D, 1.0, -1.0)
     torch.cuda.synchronize()
     ref = oracle.gemm(bits_of(A), bits_of(B), bits_of(C), M, N, K, L, 1.0, -1.0)
     assert_gemm_close(bits_of(D), ref, K, "D is C")
@@ -143,16 +162,16 @@ def test_empty_problem_is_a_no_op(gw):
     assert torch.all(D2 == 3.0)
 
 
-def test_repeated_runs_are_identical(gw):
+def test_repeated_runs_are_identical(gw_each):
     """Shakes out mbarrier phase bugs: many back-to-back launches, same bits."""
     M, N, K, L = 640, 1280, 320, 1
     A, B, _ = workloads.make_inputs(M, N, K, L, ("uniform",), None, 21)
     Ad, Bd = A.cuda(), B.cuda()
     first = torch.empty(L, M, N, dtype=torch.bfloat16, device="cuda")
-    gw.run(Ad, Bd, None, first, 1.0, 0.0)
+    gw_each.run(Ad, Bd, None, first, 1.0, 0.0)
     D = torch.empty_like(first)
     for _ in range(30):
-        gw.run(Ad, Bd, None, D, 1.0, 0.0)
+        gw_each.run(Ad, Bd, None, D, 1.0, 0.0)
     torch.cuda.synchronize()
     assert torch.equal(first.view(torch.int16), D.view(torch.int16))
     ref = oracle.gemm(bits_of(A), bits_of(B), None, M, N, K, L, 1.0, 0.0)

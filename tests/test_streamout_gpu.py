@@ -7,6 +7,7 @@ with zeros outside M and N; the sequence numbers must be a permutation of
 """
 from __future__ import annotations
 
+import os
 import numpy as np
 import pytest
 import torch
@@ -23,6 +24,24 @@ T_EDGE = 128
 @pytest.fixture(scope="module")
 def gw():
     g = gemm_ws.GemmWS(0)
+    yield g
+    assert g.query_status() == gemm_ws.OK
+    g.close()
+
+
+@pytest.fixture(scope="module", params=[2, 1], ids=["cta_pair", "cta_single"])
+def gw_each(request):
+    """A handle per tile configuration: CTA-pair 256x256 tiles (the default)
+    and single-CTA 128x256 tiles (selected at create time by the environment)."""
+    old = os.environ.get("GEMM_WS_CTA_GROUP")
+    os.environ["GEMM_WS_CTA_GROUP"] = str(request.param)
+    try:
+        g = gemm_ws.GemmWS(0)
+    finally:
+        if old is None:
+            del os.environ["GEMM_WS_CTA_GROUP"]
+        else:
+            os.environ["GEMM_WS_CTA_GROUP"] = old
     yield g
     assert g.query_status() == gemm_ws.OK
     g.close()
@@ -55,7 +74,7 @@ def check_staging(D: torch.Tensor, staging: torch.Tensor, flags: torch.Tensor):
     (256, 2904, 64, 1, 0.5),    # N edge where a 256-wide tile holds one 128 stream-out tile
     (1024, 2048, 192, 1, 0.0),  # 128 output tiles, several per CTA
 ])
-def test_streamout_small(gw, M, N, K, L, beta):
+def test_streamout_small(gw_each, M, N, K, L, beta):
     cd = ("uniform",) if beta != 0 else None
     A, B, C = workloads.make_inputs(M, N, K, L, ("uniform",), cd, seed=M + N)
     Ad, Bd = A.cuda(), B.cuda()
@@ -65,7 +84,7 @@ def test_streamout_small(gw, M, N, K, L, beta):
     staging = torch.full((T * T_EDGE * T_EDGE + 4096,), -2.0, dtype=torch.bfloat16, device="cuda")
     flags = torch.full((2 * T + 64,), 0x5A5A5A5A, dtype=torch.int32, device="cuda")
     D = torch.empty(L, M, N, dtype=torch.bfloat16, device="cuda")
-    gw.run_streamout(Ad, Bd, Cd, D, staging, flags, 1.0, beta)
+    gw_each.run_streamout(Ad, Bd, Cd, D, staging, flags, 1.0, beta)
     torch.cuda.synchronize()
     ref = oracle.gemm(bits_of(A), bits_of(B), None if C is None else bits_of(C),
                       M, N, K, L, 1.0, beta)
@@ -75,7 +94,7 @@ def test_streamout_small(gw, M, N, K, L, beta):
     assert torch.all(flags[2 * T:] == 0x5A5A5A5A), "wrote past the flags"
 
 
-def test_streamout_matches_plain_run(gw):
+def test_streamout_matches_plain_run(gw_each):
     """Stream-out leaves D identical to a plain run, bit for bit."""
     M, N, K, L = 512, 1024, 256, 1
     A, B, _ = workloads.make_inputs(M, N, K, L, ("uniform",), None, 33)
@@ -85,9 +104,9 @@ def test_streamout_matches_plain_run(gw):
     T = gemm_ws.gemm_ws_streamout_tiles(M, N, L)
     staging = torch.empty(T * T_EDGE * T_EDGE, dtype=torch.bfloat16, device="cuda")
     flags = torch.empty(2 * T, dtype=torch.int32, device="cuda")
-    gw.run(Ad, Bd, None, D0, 1.0, 0.0)
+    gw_each.run(Ad, Bd, None, D0, 1.0, 0.0)
     for _ in range(5):   # flags and counter are reset by every call
-        gw.run_streamout(Ad, Bd, None, D1, staging, flags, 1.0, 0.0)
+        gw_each.run_streamout(Ad, Bd, None, D1, staging, flags, 1.0, 0.0)
     torch.cuda.synchronize()
     assert torch.equal(D0.view(torch.int16), D1.view(torch.int16))
     check_staging(D1, staging, flags)
