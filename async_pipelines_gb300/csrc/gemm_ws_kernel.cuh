@@ -208,6 +208,44 @@ __device__ __noinline__ bool wait_bounded(uint32_t bar, uint32_t parity, const W
   }
 }
 
+// Non-blocking cluster-scope probe.
+__device__ __forceinline__ bool mbar_test_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+template <bool kCluster>
+__device__ __noinline__ bool spin_slow(uint32_t bar, uint32_t parity, const Watchdog& wd) {
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (kCluster ? mbar_test_wait_cluster(bar, parity) : mbar_test_wait(bar, parity)) return true;
+    if ((it & 255) == 0) {
+      if (*wd.abort) return false;
+      if (global_timer_ns() - t0 > wd.limit_ns) {
+        *wd.abort = 1;
+        atomicExch(wd.status, STATUS_TIMEOUT);
+        return false;
+      }
+    }
+  }
+}
+
+// Bounded wait for the latency-critical producer and MMA threads: polls
+// without ever suspending, because the wake-up delay of a suspended try_wait
+// lands directly on the load -> MMA critical path.
+template <bool kCluster>
+__device__ __forceinline__ bool wait_spin(uint32_t bar, uint32_t parity, const Watchdog& wd) {
+  if (kCluster ? mbar_test_wait_cluster(bar, parity) : mbar_test_wait(bar, parity)) return true;
+  return spin_slow<kCluster>(bar, parity, wd);
+}
+
 // Short bounded wait used only while draining after an abort.
 __device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity) {
   const uint64_t t0 = global_timer_ns();
@@ -252,7 +290,7 @@ __device__ __forceinline__ void producer_role(const Params& p, uint32_t sbase, u
     for (int kb = 0; kb < p.num_kb; ++kb) {
       const uint32_t s = g % C::STAGES;
       const uint32_t ph = (g / C::STAGES) & 1;
-      if (!token && !wait_bounded<false>(empty(s), ph ^ 1, wd)) {
+      if (!token && !wait_spin<false>(empty(s), ph ^ 1, wd)) {
         ok = false;
         break;
       }
@@ -302,14 +340,15 @@ __device__ __forceinline__ void mma_role(const Params& p, uint32_t sbase, uint32
   bool issued = false;
   for (int t = cluster; t < p.num_tiles; t += clusters, ++i) {
     const uint32_t b = i & 1, aph = (i >> 1) & 1;
-    if (!wait_bounded<true>(bar(BAR_ACC_EMPTY + b), aph ^ 1, wd)) goto done;
-    tc_fence_after_sync();
+    if (!wait_spin<true>(bar(BAR_ACC_EMPTY + b), aph ^ 1, wd)) goto done;
+    tc_fence_after_sync();   // epilogue's TMEM reads of buffer b precede these MMAs
     {
       const uint32_t d_tmem = tmem_base + b * BN;
       for (int kb = 0; kb < p.num_kb; ++kb) {
         const uint32_t s = g % C::STAGES;
-        if (!wait_bounded<true>(bar(BAR_FULL + s), (g / C::STAGES) & 1, wd)) goto done;
-        tc_fence_after_sync();
+        // The stage's bytes are ordered before the MMA by the barrier's
+        // transaction count (TMA and tcgen05 both act in the async proxy).
+        if (!wait_spin<true>(bar(BAR_FULL + s), (g / C::STAGES) & 1, wd)) goto done;
         const uint32_t a_addr = sbase + C::OFF_A + s * A_STAGE_BYTES;
         const uint32_t b_addr = sbase + C::OFF_B + s * C::B_STAGE_BYTES;
 #pragma unroll
