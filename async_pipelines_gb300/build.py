@@ -15,9 +15,12 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libgemm_ws.so")
+# Debug build: the same sources with the test hooks of include/gemm_ws_debug.h
+# (fault injection for the watchdog, per-tile timestamps). Tests only.
+DEBUG_LIB = os.path.join(PKG, "libgemm_ws_debug.so")
 SOURCES = [os.path.join(CSRC, "gemm_ws.cu")]
 DEPS = SOURCES + [os.path.join(CSRC, f) for f in ("ptx.cuh", "gemm_ws_kernel.cuh")] + [
-    os.path.join(INCLUDE, "gemm_ws.h")]
+    os.path.join(INCLUDE, "gemm_ws.h"), os.path.join(INCLUDE, "gemm_ws_debug.h")]
 
 ARCH = "-gencode=arch=compute_103a,code=sm_103a"
 
@@ -36,17 +39,28 @@ def stale(out: str = LIB) -> bool:
     return any(os.path.getmtime(d) > t for d in DEPS if os.path.exists(d))
 
 
-def build(out: str = LIB, extra=(), verbose: bool = False) -> str:
+def _cmd(out: str, extra=(), verbose: bool = False):
     cmd = [nvcc(), ARCH, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-shared",
            f"-I{INCLUDE}", "-o", out, *extra, *SOURCES]
     if verbose:
         cmd.insert(1, "-Xptxas=-v")
-    subprocess.run(cmd, check=True)
+    return cmd
+
+
+def build(out: str = LIB, extra=(), verbose: bool = False, debug: bool = True) -> str:
+    """Builds the production library (and, by default, the debug library) in
+    parallel nvcc processes."""
+    procs = [subprocess.Popen(_cmd(out, extra, verbose))]
+    if debug:
+        procs.append(subprocess.Popen(_cmd(DEBUG_LIB, ("-DGEMM_WS_DEBUG", *extra))))
+    codes = [p.wait() for p in procs]
+    if any(codes):
+        raise subprocess.CalledProcessError(max(codes), "nvcc")
     return out
 
 
 def ensure_built() -> str:
-    if stale():
+    if stale() or stale(DEBUG_LIB):
         build()
     return LIB
 

@@ -12,6 +12,9 @@
 #include <mutex>
 
 #include "gemm_ws.h"
+#ifdef GEMM_WS_DEBUG
+#include "gemm_ws_debug.h"
+#endif
 #include "gemm_ws_kernel.cuh"
 
 struct gemm_ws {
@@ -24,6 +27,10 @@ struct gemm_ws {
   int last_cuda_error;
   unsigned long long timeout_ns;
   PFN_cuTensorMapEncodeTiled_v12000 encode;
+#ifdef GEMM_WS_DEBUG
+  int debug_fault;
+  unsigned long long* trace;
+#endif
 };
 
 namespace {
@@ -164,6 +171,10 @@ int launch(gemm_ws* h, const uint16_t* A, const uint16_t* B, const uint16_t* C, 
   p.counter = h->work;
   p.status = h->work + 1;
   p.timeout_ns = h->timeout_ns;
+#ifdef GEMM_WS_DEBUG
+  p.debug_fault = h->debug_fault;
+  p.trace = h->trace;
+#endif
 
   cudaError_t e;
   if (staging) {
@@ -354,6 +365,29 @@ const char* gemm_ws_status_string(int status) {
   }
 }
 
+#ifdef GEMM_WS_DEBUG
+int gemm_ws_debug_configure(gemm_ws_t* h, int fault, unsigned long long* trace) {
+  if (!h || fault < 0 || fault > 1) return GEMM_WS_ERR_INVALID_ARG;
+  h->debug_fault = fault;
+  h->trace = trace;
+  return GEMM_WS_OK;
+}
+
+int gemm_ws_debug_launch_shape(gemm_ws_t* h, int64_t M, int64_t N, int64_t L, int* cta_group,
+                               int* clusters, int* num_tiles) {
+  if (!h || !cta_group || !clusters || !num_tiles || M <= 0 || N <= 0 || L <= 0)
+    return GEMM_WS_ERR_INVALID_ARG;
+  const int cg = h->cta_group;
+  const int64_t tiles =
+      L * ((M + gws::BM * cg - 1) / (gws::BM * cg)) * ((N + gws::BN - 1) / gws::BN);
+  const int64_t cap = cg == 1 ? h->num_sms : h->max_pair_clusters;
+  *cta_group = cg;
+  *num_tiles = static_cast<int>(tiles);
+  *clusters = static_cast<int>(tiles < cap ? tiles : cap);
+  return GEMM_WS_OK;
+}
+#endif
+
 int64_t gemm_ws_streamout_tiles(int64_t M, int64_t N, int64_t L) {
   if (M <= 0 || N <= 0 || L <= 0) return 0;
   return L * ((M + gws::STAGING - 1) / gws::STAGING) * ((N + gws::STAGING - 1) / gws::STAGING);
@@ -386,6 +420,10 @@ struct NoAllocDevice {
   uint32_t* scratch;   // device address of g_noalloc_scratch on this device
   unsigned long long timeout_ns;
   PFN_cuTensorMapEncodeTiled_v12000 encode;
+#ifdef GEMM_WS_DEBUG
+  int debug_fault;
+  unsigned long long* trace;
+#endif
 };
 
 NoAllocDevice g_noalloc_devices[kNoAllocMaxDevices];

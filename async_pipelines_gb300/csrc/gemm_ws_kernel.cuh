@@ -136,6 +136,10 @@ struct Params {
   uint32_t* counter;             // stream-out sequence counter (zeroed by host)
   uint32_t* status;              // watchdog status word
   unsigned long long timeout_ns; // bound of every single wait
+#ifdef GEMM_WS_DEBUG
+  int debug_fault;               // 1: the stream-out consumer takes no tile
+  unsigned long long* trace;     // [tile][CG][2] global-timer stamps, or null
+#endif
 };
 
 // Tile t -> (m block, n block, batch). Within a batch, tiles go down a group
@@ -455,6 +459,11 @@ __device__ __forceinline__ void epilogue_role(const Params& p, uint32_t sbase, u
 
     if (!warp_wait(bar(BAR_ACC_FULL + b), aph, wd)) break;
     tc_fence_after_sync();
+#ifdef GEMM_WS_DEBUG
+    // stamp 0: this CTA's part of tile t has its accumulator (MMA done)
+    if (p.trace && q == (WARP_EPI0 & 3) && lane == 0)
+      p.trace[(static_cast<size_t>(t) * CG + rank) * 2] = global_timer_ns();
+#endif
     const uint32_t tacc = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + b * BN;
     if (nsub == 0) release_acc();   // this CTA's rows lie outside M
 
@@ -543,6 +552,9 @@ __device__ __forceinline__ void consumer_role(const Params& p, uint32_t sbase, u
   using C = Cfg<CG>;
   auto bar = [&](int i) { return sbase + C::OFF_BAR + 8 * i; };
   const int cluster = blockIdx.x / CG, clusters = gridDim.x / CG;
+#ifdef GEMM_WS_DEBUG
+  if (p.debug_fault == 1) return;   // injected fault: no tile is ever taken
+#endif
   uint32_t u = 0;
   for (int t = cluster; t < p.num_tiles; t += clusters) {
     int mb, nb, l;
@@ -570,6 +582,11 @@ __device__ __forceinline__ void consumer_role(const Params& p, uint32_t sbase, u
       st_relaxed_gpu(p.flags + 2 * tile_id, seq);
       st_release_gpu(p.flags + 2 * tile_id + 1, 1u);
     }
+#ifdef GEMM_WS_DEBUG
+    // stamp 1: every stream-out tile of this CTA's part of tile t is published
+    if (p.trace && nst > 0)
+      p.trace[(static_cast<size_t>(t) * CG + rank) * 2 + 1] = global_timer_ns();
+#endif
   }
 done:
   bulk_wait<0>();

@@ -81,6 +81,26 @@ def load_library(path: Optional[str] = None):
     return lib
 
 
+DEBUG_EXPORTS = ("gemm_ws_debug_configure", "gemm_ws_debug_launch_shape")
+
+_debug_lib = None
+
+
+def load_debug_library():
+    """The debug build (test hooks of include/gemm_ws_debug.h). Tests only."""
+    global _debug_lib
+    if _debug_lib is None:
+        lib = load_library(_build.DEBUG_LIB)
+        lib.gemm_ws_debug_configure.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p]
+        lib.gemm_ws_debug_configure.restype = ctypes.c_int
+        ip = ctypes.POINTER(ctypes.c_int)
+        lib.gemm_ws_debug_launch_shape.argtypes = [ctypes.c_void_p, ctypes.c_int64,
+                                                   ctypes.c_int64, ctypes.c_int64, ip, ip, ip]
+        lib.gemm_ws_debug_launch_shape.restype = ctypes.c_int
+        _debug_lib = lib
+    return _debug_lib
+
+
 def status_string(status: int) -> str:
     return load_library().gemm_ws_status_string(int(status)).decode()
 
@@ -163,15 +183,23 @@ def _check_operands(A, B, C, D):
 
 
 class GemmWS:
-    """Owns one library handle on one CUDA device."""
+    """Owns one library handle on one CUDA device.
 
-    def __init__(self, device: int = 0):
+    `lib` selects the loaded library (default: the production build; tests
+    pass the debug build from `load_debug_library()`)."""
+
+    def __init__(self, device: int = 0, lib=None):
         self.device = int(device)
-        self.handle = gemm_ws_create(self.device)
+        self.lib = lib or load_library()
+        h = ctypes.c_void_p()
+        rc = self.lib.gemm_ws_create(ctypes.byref(h), self.device)
+        if rc != OK:
+            raise GemmWSError(rc, "gemm_ws_create")
+        self.handle = h
 
     def close(self):
         if self.handle is not None:
-            gemm_ws_destroy(self.handle)
+            self.lib.gemm_ws_destroy(self.handle)
             self.handle = None
 
     def __del__(self):
@@ -182,7 +210,7 @@ class GemmWS:
 
     def _raise(self, rc, what):
         if rc != OK:
-            raise GemmWSError(rc, what, gemm_ws_last_cuda_error(self.handle))
+            raise GemmWSError(rc, what, self.lib.gemm_ws_last_cuda_error(self.handle))
 
     def run(self, A, B, C, D, alpha=1.0, beta=0.0, stream=None):
         """D = alpha * A @ B^T-stored + beta * C on the current (or given) stream.
@@ -190,8 +218,9 @@ class GemmWS:
         A: (L, M, K), B: (L, N, K) (column-major K x N per batch), C/D: (L, M, N).
         """
         M, N, K, L = _check_operands(A, B, C, D)
-        self._raise(gemm_ws_run(self.handle, A, B, C, D, M, N, K, L, alpha, beta, stream),
-                    "gemm_ws_run")
+        rc = self.lib.gemm_ws_run(self.handle, _ptr(A), _ptr(B), _ptr(C), _ptr(D), M, N, K, L,
+                                  float(alpha), float(beta), _stream(stream))
+        self._raise(rc, "gemm_ws_run")
         return D
 
     def run_streamout(self, A, B, C, D, staging, flags, alpha=1.0, beta=0.0, stream=None):
@@ -201,9 +230,11 @@ class GemmWS:
             raise ValueError(f"staging must be bf16 with >= {T} * 128 * 128 elements")
         if flags.dtype != torch.int32 or flags.numel() < 2 * T:
             raise ValueError(f"flags must be int32 (read as uint32) with >= {2 * T} elements")
-        self._raise(gemm_ws_run_streamout(self.handle, A, B, C, D, M, N, K, L, alpha, beta,
-                                          staging, flags, stream), "gemm_ws_run_streamout")
+        rc = self.lib.gemm_ws_run_streamout(self.handle, _ptr(A), _ptr(B), _ptr(C), _ptr(D), M,
+                                            N, K, L, float(alpha), float(beta), _ptr(staging),
+                                            _ptr(flags), _stream(stream))
+        self._raise(rc, "gemm_ws_run_streamout")
         return D
 
     def query_status(self, stream=None) -> int:
-        return gemm_ws_query_status(self.handle, stream)
+        return self.lib.gemm_ws_query_status(self.handle, _stream(stream))

@@ -1,0 +1,49 @@
+/*
+ * gemm_ws_debug.h — test hooks of the debug build of the GEMM library
+ * (libgemm_ws_debug.so, compiled with -DGEMM_WS_DEBUG). The production
+ * library (libgemm_ws.so) does not export these functions.
+ *
+ * The hooks serve two checks:
+ *  - the watchdog: a run whose stream-out consumer warp never takes a tile
+ *    must end on its own, report GEMM_WS_ERR_TIMEOUT through
+ *    gemm_ws_query_status, and leave the device usable;
+ *  - overlap of the tile handoff with compute, the property the issue
+ *    "How to build a pipeline between epilogue and communication warp
+ *    groups?" asks to be shown: per-tile global-timer stamps of "accumulator
+ *    complete" and "tile published".
+ */
+#ifndef GEMM_WS_DEBUG_H_
+#define GEMM_WS_DEBUG_H_
+
+#include <stdint.h>
+
+#include "gemm_ws.h"
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Sets the handle's debug state for its later runs.
+ *  - fault: 0 none; 1 the stream-out consumer warp returns at once, so the
+ *    epilogue's wait for a free slot can only end by the watchdog.
+ *  - trace: device buffer of num_tiles * cta_group * 2 uint64 (see
+ *    gemm_ws_debug_launch_shape) or NULL. For tile t and CTA rank r of its
+ *    CTA group, trace[(t*cta_group + r)*2] = global time (ns) at which that
+ *    CTA's epilogue saw the tile's accumulator complete, and [...+1] = time at
+ *    which its consumer published the last stream-out tile of that part
+ *    (written only by gemm_ws_run_streamout; untouched where the part lies
+ *    outside M). The caller owns the buffer.
+ * Returns GEMM_WS_OK or GEMM_WS_ERR_INVALID_ARG. */
+int gemm_ws_debug_configure(gemm_ws_t* h, int fault, unsigned long long* trace);
+
+/* The launch the handle would make for an M x N x L problem: CTA group size
+ * (1 or 2), number of clusters (persistent CTA groups; cluster c takes tiles
+ * c, c + clusters, ...) and number of tiles. Host arithmetic only. */
+int gemm_ws_debug_launch_shape(gemm_ws_t* h, int64_t M, int64_t N, int64_t L,
+                               int* cta_group, int* clusters, int* num_tiles);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GEMM_WS_DEBUG_H_ */

@@ -1,0 +1,44 @@
+"""Debug-build plumbing for the watchdog and overlap tests."""
+from __future__ import annotations
+
+import contextlib
+import ctypes
+import os
+
+from async_pipelines_gb300 import gemm_ws
+
+
+@contextlib.contextmanager
+def env(**kv):
+    old = {k: os.environ.get(k) for k in kv}
+    os.environ.update({k: str(v) for k, v in kv.items()})
+    try:
+        yield
+    finally:
+        for k, v in old.items():
+            if v is None:
+                os.environ.pop(k, None)
+            else:
+                os.environ[k] = v
+
+
+def debug_handle(cta_group: int = 2, timeout_ms: int = 1000) -> gemm_ws.GemmWS:
+    """A handle on the debug build, created with the given tile configuration
+    and per-wait watchdog limit."""
+    lib = gemm_ws.load_debug_library()
+    with env(GEMM_WS_CTA_GROUP=cta_group, GEMM_WS_TIMEOUT_MS=timeout_ms):
+        return gemm_ws.GemmWS(0, lib=lib)
+
+
+def launch_shape(g: gemm_ws.GemmWS, M: int, N: int, L: int):
+    cg, cl, nt = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+    rc = g.lib.gemm_ws_debug_launch_shape(g.handle, M, N, L, ctypes.byref(cg),
+                                          ctypes.byref(cl), ctypes.byref(nt))
+    assert rc == gemm_ws.OK
+    return cg.value, cl.value, nt.value
+
+
+def configure(g: gemm_ws.GemmWS, fault: int, trace_ptr=None):
+    rc = g.lib.gemm_ws_debug_configure(g.handle, fault,
+                                       None if trace_ptr is None else ctypes.c_void_p(trace_ptr))
+    assert rc == gemm_ws.OK

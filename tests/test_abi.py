@@ -16,8 +16,11 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADER = os.path.join(ROOT, "include", "gemm_ws.h")
 
 
-def declared_functions():
-    text = open(HEADER).read()
+DEBUG_HEADER = os.path.join(ROOT, "include", "gemm_ws_debug.h")
+
+
+def declared_functions(header=HEADER):
+    text = open(header).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
     return sorted(set(re.findall(r"\b(gemm_ws_\w+)\s*\(", text)))
 
@@ -39,6 +42,17 @@ def test_library_exports_every_declared_function(lib):
     for name in declared_functions():
         assert hasattr(lib, name), f"{name} declared in gemm_ws.h but not exported"
     assert set(declared_functions()) == set(gemm_ws.EXPORTS)
+
+
+def test_debug_hooks_only_in_the_debug_build(lib):
+    import ctypes
+    dbg = ctypes.CDLL(build.DEBUG_LIB)
+    debug_names = [n for n in declared_functions(DEBUG_HEADER) if n.startswith("gemm_ws_debug")]
+    assert set(debug_names) == set(gemm_ws.DEBUG_EXPORTS)
+    for name in declared_functions() + debug_names:
+        assert hasattr(dbg, name), name
+    for name in debug_names:
+        assert not hasattr(lib, name), f"{name} leaked into the production library"
 
 
 def test_streamout_tile_count_is_host_arithmetic(lib):

@@ -1,0 +1,53 @@
+"""The watchdog, tested without faulting the GPU.
+
+The debug build's fault switch makes the stream-out consumer warp take no
+tile, so the epilogue's wait for a free shared-memory slot is a wait on a
+barrier that nothing will ever complete. The run must end on its own within
+its bounded waits, report GEMM_WS_ERR_TIMEOUT through the status query, and
+leave the device usable: the next normal run on the same handle is correct.
+"""
+from __future__ import annotations
+
+import time
+
+import pytest
+import torch
+
+import oracle
+from async_pipelines_gb300 import gemm_ws, workloads
+from tests.debug_helpers import configure, debug_handle
+from tests.gpu_helpers import bits_of
+from tests.numerics import assert_gemm_close
+from tests.test_streamout_gpu import check_staging
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("cta_group", [2, 1])
+def test_consumer_that_takes_no_tile_times_out_then_recovers(cta_group):
+    g = debug_handle(cta_group=cta_group, timeout_ms=200)
+    M, N, K, L = 512, 512, 128, 1
+    A, B, _ = workloads.make_inputs(M, N, K, L, ("uniform",), None, seed=41)
+    Ad, Bd = A.cuda(), B.cuda()
+    T = gemm_ws.gemm_ws_streamout_tiles(M, N, L)
+    staging = torch.empty(T * 128 * 128, dtype=torch.bfloat16, device="cuda")
+    flags = torch.empty(2 * T, dtype=torch.int32, device="cuda")
+    D = torch.empty(L, M, N, dtype=torch.bfloat16, device="cuda")
+
+    configure(g, fault=1)
+    t0 = time.perf_counter()
+    g.run_streamout(Ad, Bd, None, D, staging, flags, 1.0, 0.0)
+    status = g.query_status()
+    elapsed = time.perf_counter() - t0
+    assert status == gemm_ws.ERR_TIMEOUT, gemm_ws.status_string(status)
+    assert elapsed < 20.0
+    assert g.query_status() == gemm_ws.OK          # reading cleared the word
+    assert int(flags[1::2].sum().item()) == 0      # no tile was flagged ready
+
+    configure(g, fault=0)
+    g.run_streamout(Ad, Bd, None, D, staging, flags, 1.0, 0.0)
+    assert g.query_status() == gemm_ws.OK
+    ref = oracle.gemm(bits_of(A), bits_of(B), None, M, N, K, L, 1.0, 0.0)
+    assert_gemm_close(bits_of(D), ref, K, "after recovery")
+    check_staging(D, staging, flags)
+    g.close()
