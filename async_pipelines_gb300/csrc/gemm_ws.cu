@@ -87,6 +87,32 @@ int check_problem(gemm_ws* h, const uint16_t* A, const uint16_t* B, const uint16
   return GEMM_WS_OK;
 }
 
+// How many of the last tiles (in raster order) to run as two half-width
+// units so that the persistent schedule's final wave is not half idle.
+// Cluster c runs units c, c + P, ...; a whole tile costs 1, a half ~0.6 (same
+// k-loop and A traffic, half the MMA work). Returns the number of whole
+// tiles; only splits of at most one wave of tiles are considered.
+int64_t choose_num_full(int64_t tiles, int64_t P) {
+  if (P <= 1 || tiles <= P) return tiles;
+  double best = 0.0;
+  int64_t best_full = tiles;
+  for (int64_t s = 0; s <= P && s <= tiles; ++s) {
+    const int64_t F = tiles - s, U = F + 2 * s;
+    double worst = 0.0;
+    for (int64_t c = 0; c < P; ++c) {
+      const int64_t n_units = U / P + (c < U % P ? 1 : 0);
+      const int64_t n_full = F / P + (c < F % P ? 1 : 0);
+      const double t = static_cast<double>(n_full) + 0.6 * static_cast<double>(n_units - n_full);
+      if (t > worst) worst = t;
+    }
+    if (s == 0 || worst < best - 1e-9) {
+      best = worst;
+      best_full = F;
+    }
+  }
+  return best_full;
+}
+
 // Sets the shared-memory attribute of both kernel instances on the current
 // device and returns how many 2-CTA clusters of the pair kernel fit at once.
 cudaError_t configure_kernels(int num_sms, int* max_pair_clusters) {
@@ -136,6 +162,9 @@ int launch(gemm_ws* h, const uint16_t* A, const uint16_t* B, const uint16_t* C, 
     if (r == CUDA_SUCCESS)
       r = encode3d(h, &p.tmB, B, K, N, L, gws::BK, gws::BN / cg, CU_TENSOR_MAP_SWIZZLE_128B,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+    if (r == CUDA_SUCCESS)
+      r = encode3d(h, &p.tmB2, B, K, N, L, gws::BK, gws::BN / 2 / cg,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
   }
   if (r == CUDA_SUCCESS && beta != 0.0f)
     r = encode3d(h, &p.tmC, C, N, M, L, gws::EPI_N, 32, CU_TENSOR_MAP_SWIZZLE_64B,
@@ -159,6 +188,12 @@ int launch(gemm_ws* h, const uint16_t* A, const uint16_t* B, const uint16_t* C, 
   p.tiles_m = static_cast<int>(tiles_m);
   p.tiles_n = static_cast<int>(tiles_n);
   p.num_tiles = static_cast<int>(num_tiles);
+  const int64_t P = cg == 1 ? h->num_sms : h->max_pair_clusters;
+  const int64_t num_full = choose_num_full(num_tiles, P);
+  const int64_t num_units = num_full + 2 * (num_tiles - num_full);
+  if (num_units > kMaxDim) return GEMM_WS_ERR_INVALID_ARG;
+  p.num_full = static_cast<int>(num_full);
+  p.num_units = static_cast<int>(num_units);
   p.num_kb = static_cast<int>((K + gws::BK - 1) / gws::BK);
   p.group_m = h->group_m;
   p.staging_tiles_m = static_cast<int>((M + gws::STAGING - 1) / gws::STAGING);
@@ -183,11 +218,11 @@ int launch(gemm_ws* h, const uint16_t* A, const uint16_t* B, const uint16_t* C, 
     if (e != cudaSuccess) return cuda_fail(h, e);
   }
   if (cg == 1) {
-    const int grid = static_cast<int>(num_tiles < h->num_sms ? num_tiles : h->num_sms);
+    const int grid = static_cast<int>(num_units < h->num_sms ? num_units : h->num_sms);
     gws::gemm_ws_kernel<1><<<grid, gws::NUM_THREADS, gws::Cfg<1>::SMEM_BYTES, stream>>>(p);
     e = cudaGetLastError();
   } else {
-    const int64_t clusters = num_tiles < h->max_pair_clusters ? num_tiles : h->max_pair_clusters;
+    const int64_t clusters = num_units < h->max_pair_clusters ? num_units : h->max_pair_clusters;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -381,9 +416,11 @@ int gemm_ws_debug_launch_shape(gemm_ws_t* h, int64_t M, int64_t N, int64_t L, in
   const int64_t tiles =
       L * ((M + gws::BM * cg - 1) / (gws::BM * cg)) * ((N + gws::BN - 1) / gws::BN);
   const int64_t cap = cg == 1 ? h->num_sms : h->max_pair_clusters;
+  const int64_t full = choose_num_full(tiles, cap);
+  const int64_t units = full + 2 * (tiles - full);
   *cta_group = cg;
-  *num_tiles = static_cast<int>(tiles);
-  *clusters = static_cast<int>(tiles < cap ? tiles : cap);
+  *num_tiles = static_cast<int>(units);
+  *clusters = static_cast<int>(units < cap ? units : cap);
   return GEMM_WS_OK;
 }
 #endif

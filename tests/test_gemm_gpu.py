@@ -106,6 +106,7 @@ def test_integer_inputs_bit_exact(gw_each, M, N, K, L):
     (64, 512, 56, 2, -1.25, 0.75),
     (513, 1032, 1000, 1, 1.0, 1.0),
     (4096, 4096, 128, 1, 1.0, 0.0),   # 512 tiles: several tiles per CTA
+    (4000, 4104, 96, 2, 1.0, 0.5),    # tail tiles split into halves, ragged N edge in a half
 ])
 def test_small_shapes_match_oracle(gw_each, M, N, K, L, alpha, beta):
     cd = ("normal", 1.0) if beta != 0 else None

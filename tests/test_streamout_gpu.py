@@ -73,6 +73,7 @@ def check_staging(D: torch.Tensor, staging: torch.Tensor, flags: torch.Tensor):
     (300, 392, 136, 2, 0.0),    # ragged M and N, batches
     (256, 2904, 64, 1, 0.5),    # N edge where a 256-wide tile holds one 128 stream-out tile
     (1024, 2048, 192, 1, 0.0),  # 128 output tiles, several per CTA
+    (4096, 4096, 64, 1, 0.0),   # more tiles than one wave: the last ones run as halves
 ])
 def test_streamout_small(gw_each, M, N, K, L, beta):
     cd = ("uniform",) if beta != 0 else None
