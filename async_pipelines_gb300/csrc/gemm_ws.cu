@@ -23,7 +23,8 @@ struct gemm_ws {
   int cta_group;                  // 2: CTA-pair tiles (default); 1: single-CTA tiles
   int group_m;                    // raster group: m-tiles walked per n step
   int max_pair_clusters;          // co-resident 2-CTA clusters of the pair kernel
-  uint32_t* work;                 // [0] stream-out counter, [1] status word
+  uint32_t* work;                 // [0], [2] stream-out counters, [1] status word
+  uint32_t counter_parity;        // which counter the next stream-out launch uses
   int last_cuda_error;
   unsigned long long timeout_ns;
   PFN_cuTensorMapEncodeTiled_v12000 encode;
@@ -37,6 +38,7 @@ namespace {
 
 constexpr int64_t kMaxDim = (int64_t{1} << 31) - 1;
 constexpr int64_t kMaxElems = int64_t{1} << 40;
+constexpr int kWorkWords = 4;   // counters at [0] and [2], status at [1]
 
 int cuda_fail(gemm_ws* h, cudaError_t e) {
   if (h) h->last_cuda_error = static_cast<int>(e);
@@ -203,7 +205,8 @@ int launch(gemm_ws* h, const uint16_t* A, const uint16_t* B, const uint16_t* C, 
   p.has_c = beta != 0.0f ? 1 : 0;
   p.streamout = staging ? 1 : 0;
   p.flags = flags;
-  p.counter = h->work;
+  p.counter = h->work + (h->counter_parity ? 2 : 0);
+  p.counter_next = h->work + (h->counter_parity ? 0 : 2);
   p.status = h->work + 1;
   p.timeout_ns = h->timeout_ns;
 #ifdef GEMM_WS_DEBUG
@@ -212,11 +215,6 @@ int launch(gemm_ws* h, const uint16_t* A, const uint16_t* B, const uint16_t* C, 
 #endif
 
   cudaError_t e;
-  if (staging) {
-    e = cudaMemsetAsync(flags, 0, static_cast<size_t>(2 * T) * sizeof(uint32_t), stream);
-    if (e == cudaSuccess) e = cudaMemsetAsync(h->work, 0, sizeof(uint32_t), stream);
-    if (e != cudaSuccess) return cuda_fail(h, e);
-  }
   if (cg == 1) {
     const int grid = static_cast<int>(num_units < h->num_sms ? num_units : h->num_sms);
     gws::gemm_ws_kernel<1><<<grid, gws::NUM_THREADS, gws::Cfg<1>::SMEM_BYTES, stream>>>(p);
@@ -238,6 +236,7 @@ int launch(gemm_ws* h, const uint16_t* A, const uint16_t* B, const uint16_t* C, 
     e = cudaLaunchKernelEx(&cfg, gws::gemm_ws_kernel<2>, p);
   }
   if (e != cudaSuccess) return cuda_fail(h, e);
+  if (staging) h->counter_parity ^= 1u;   // this launch zeroed the other counter
   return GEMM_WS_OK;
 }
 
@@ -315,8 +314,8 @@ int gemm_ws_create(gemm_ws_t** out, int device) {
   h->group_m = group_m_from_env();
   e = configure_kernels(h->num_sms, &h->max_pair_clusters);
   if (e == cudaSuccess && h->max_pair_clusters < 1) h->cta_group = 1;
-  if (e == cudaSuccess) e = cudaMalloc(&h->work, 2 * sizeof(uint32_t));
-  if (e == cudaSuccess) e = cudaMemset(h->work, 0, 2 * sizeof(uint32_t));
+  if (e == cudaSuccess) e = cudaMalloc(&h->work, kWorkWords * sizeof(uint32_t));
+  if (e == cudaSuccess) e = cudaMemset(h->work, 0, kWorkWords * sizeof(uint32_t));
   if (e != cudaSuccess) {
     if (h->work) cudaFree(h->work);
     std::free(h);
@@ -451,6 +450,7 @@ constexpr int kNoAllocMaxDevices = 64;
 
 struct NoAllocDevice {
   bool ready;
+  uint32_t counter_parity;
   int num_sms;
   int cta_group;
   int max_pair_clusters;
@@ -468,7 +468,8 @@ std::mutex g_noalloc_mutex;
 
 }  // namespace
 
-// word 0: stream-out sequence counter; word 1: watchdog status.
+// words 0 and 2: the two alternating stream-out sequence counters (each
+// launch zeroes the one the next launch uses); word 1: watchdog status.
 static __device__ __align__(256) uint32_t g_noalloc_scratch[kNoAllocScratchWords];
 
 namespace {
@@ -532,6 +533,7 @@ extern "C" int gemm_ws_run_streamout_noalloc(const uint16_t* A, const uint16_t* 
   NoAllocDevice* d = nullptr;
   int rc = noalloc_setup(device, &d);
   if (rc != GEMM_WS_OK) return rc;
+  std::lock_guard<std::mutex> lock(g_noalloc_mutex);   // the counter parity is shared
   gemm_ws h;   // a handle on the host stack that borrows the static scratch
   std::memset(&h, 0, sizeof h);
   h.device = device;
@@ -542,5 +544,8 @@ extern "C" int gemm_ws_run_streamout_noalloc(const uint16_t* A, const uint16_t* 
   h.work = d->scratch;
   h.timeout_ns = d->timeout_ns;
   h.encode = d->encode;
-  return gemm_ws_run_streamout(&h, A, B, C, D, M, N, K, L, alpha, beta, staging, flags, stream);
+  h.counter_parity = d->counter_parity;
+  rc = gemm_ws_run_streamout(&h, A, B, C, D, M, N, K, L, alpha, beta, staging, flags, stream);
+  d->counter_parity = h.counter_parity;
+  return rc;
 }

@@ -145,7 +145,8 @@ struct Params {
   int has_c;                     // beta != 0
   int streamout;
   uint32_t* flags;               // 2 * T words (stream-out)
-  uint32_t* counter;             // stream-out sequence counter (zeroed by host)
+  uint32_t* counter;             // stream-out sequence counter (zero at launch)
+  uint32_t* counter_next;        // the other counter: zeroed here for the next launch
   uint32_t* status;              // watchdog status word
   unsigned long long timeout_ns; // bound of every single wait
 #ifdef GEMM_WS_DEBUG
@@ -302,6 +303,18 @@ __device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity) {
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const Watchdog& wd) {
   uint32_t ok = 0;
   if ((threadIdx.x & 31) == 0) ok = wait_bounded<true>(bar, parity, wd) ? 1u : 0u;
+  ok = __shfl_sync(0xffffffffu, ok, 0);
+  if (ok) (void)mbar_try_wait_cluster(bar, parity);
+  __syncwarp();
+  return ok != 0;
+}
+
+// Warp-uniform wait for the epilogue's short, latency-critical handoffs (C
+// arrival, a free D slot): lane 0 polls without suspending.
+__device__ __forceinline__ bool warp_wait_spin(uint32_t bar, uint32_t parity,
+                                               const Watchdog& wd) {
+  uint32_t ok = 0;
+  if ((threadIdx.x & 31) == 0) ok = wait_spin<true>(bar, parity, wd) ? 1u : 0u;
   ok = __shfl_sync(0xffffffffu, ok, 0);
   if (ok) (void)mbar_try_wait_cluster(bar, parity);
   __syncwarp();
@@ -536,7 +549,7 @@ __device__ __forceinline__ void epilogue_role(const Params& p, uint32_t sbase, u
       for (int e = 0; e < 32; ++e) v[e] = p.alpha * __uint_as_float(acc[e]);
       if (p.has_c) {
         const uint32_t cb = cu % C_BUFS;
-        if (!warp_wait(bar(BAR_C_FULL + q * C_BUFS + cb), (cu / C_BUFS) & 1, wd)) {
+        if (!warp_wait_spin(bar(BAR_C_FULL + q * C_BUFS + cb), (cu / C_BUFS) & 1, wd)) {
           ok = false;
           break;
         }
@@ -558,7 +571,7 @@ __device__ __forceinline__ void epilogue_role(const Params& p, uint32_t sbase, u
       const uint32_t slot = u % EPI_SLOTS;
       if (lane == 0) bulk_wait_read<EPI_SLOTS - 1>();
       if (p.streamout) {
-        if (!warp_wait(bar(BAR_D_EMPTY + slot), ((u / EPI_SLOTS) & 1) ^ 1, wd)) {
+        if (!warp_wait_spin(bar(BAR_D_EMPTY + slot), ((u / EPI_SLOTS) & 1) ^ 1, wd)) {
           ok = false;
           break;
         }
@@ -602,6 +615,23 @@ __device__ __forceinline__ void consumer_role(const Params& p, uint32_t sbase, u
   using C = Cfg<CG>;
   auto bar = [&](int i) { return sbase + C::OFF_BAR + 8 * i; };
   const int cluster = blockIdx.x / CG, clusters = gridDim.x / CG;
+  // Each stream-out tile has exactly one publishing consumer, which clears
+  // the tile's flag words before anything else; so no host-side clearing is
+  // needed and nothing in this launch can observe a stale ready word. The
+  // first CTA also zeroes the counter that the NEXT launch will use (stream
+  // order makes that visible to it).
+  if (blockIdx.x == 0) st_relaxed_gpu(p.counter_next, 0u);
+  for (int t = cluster; t < p.num_units; t += clusters) {
+    const Unit w = unit_coords(p, t);
+    const int row_tile = w.mb * CG + static_cast<int>(rank);
+    const int nst = staging_in_part(p, row_tile, w);
+    for (int st = 0; st < nst; ++st) {
+      const int tile_id =
+          (w.l * p.staging_tiles_m + row_tile) * p.staging_tiles_n + w.n0 / STAGING + st;
+      st_relaxed_gpu(p.flags + 2 * tile_id, 0u);
+      st_relaxed_gpu(p.flags + 2 * tile_id + 1, 0u);
+    }
+  }
 #ifdef GEMM_WS_DEBUG
   if (p.debug_fault == 1) return;   // injected fault: no tile is ever taken
 #endif
@@ -616,7 +646,7 @@ __device__ __forceinline__ void consumer_role(const Params& p, uint32_t sbase, u
       uint32_t seq = 0;
       for (int jj = 0; jj < SUB_PER_STAGING; ++jj) {
         const uint32_t slot = u % EPI_SLOTS;
-        if (!wait_bounded<false>(bar(BAR_D_FULL + slot), (u / EPI_SLOTS) & 1, wd)) goto done;
+        if (!wait_spin<false>(bar(BAR_D_FULL + slot), (u / EPI_SLOTS) & 1, wd)) goto done;
         if (jj == 0) seq = atomicAdd(p.counter, 1u);   // completion order
         tma_store_3d(&p.tmS, sbase + C::OFF_D + slot * EPI_SLOT_BYTES, jj * EPI_N, 0,
                      static_cast<int>(seq));

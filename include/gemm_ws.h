@@ -25,8 +25,8 @@
  *
  * Ownership: every data pointer is a borrowed DEVICE pointer on the handle's
  * device; the caller owns it and keeps it alive until the stream work ends.
- * The handle owns only its small device workspace (stream-out counter and
- * status word).
+ * The handle owns only its small device workspace (two stream-out counters
+ * and a status word).
  *
  * Errors: every entry point returns a gemm_ws_status. A call that returns an
  * error other than GEMM_WS_ERR_CUDA launched nothing and wrote nothing. All
@@ -89,9 +89,10 @@ int gemm_ws_run(gemm_ws_t* h, const uint16_t* A, const uint16_t* B,
  *    M or N are 0.
  *  - flags: device buffer of 2 * T uint32. After the stream work completes,
  *    flags[2t] = s (the slot / sequence number of tile t, 0-based and dense)
- *    and flags[2t+1] = 1. The library clears flags on `stream` before the
- *    launch; the ready word is written with release semantics after the
- *    tile's staging bytes are globally visible.
+ *    and flags[2t+1] = 1. Within the launch, the warp that publishes a tile
+ *    first clears that tile's two words, then writes the ready word with
+ *    release semantics after the tile's staging bytes are globally visible.
+ *    (No host-side memset: the call launches exactly one kernel.)
  *  - staging and flags must not overlap any other argument.
  * Returns as gemm_ws_run. */
 int gemm_ws_run_streamout(gemm_ws_t* h, const uint16_t* A, const uint16_t* B,
@@ -133,9 +134,11 @@ int64_t gemm_ws_streamout_tiles(int64_t M, int64_t N, int64_t L);
  *    checks, kernel attribute, address of the scratch array); make that first
  *    call before any stream capture.
  *  - Every call shares the one scratch array, which keeps the last call's
- *    contents; each call clears the counter (and the flags) on `stream`
- *    before its launch. Calls that overlap on the GPU (e.g. on two streams)
- *    race on the counter and produce wrong sequence numbers: serialise them.
+ *    contents. It holds two sequence counters used alternately: each call's
+ *    kernel zeroes the one the next call will use, so consecutive calls on
+ *    one stream need no clearing. Calls that overlap on the GPU (e.g. on two
+ *    streams) race on the counters and produce wrong sequence numbers:
+ *    serialise them.
  *  - A watchdog timeout is not reported through a status query here; it shows
  *    as tiles whose ready word flags[2t+1] stayed 0. */
 int gemm_ws_run_streamout_noalloc(const uint16_t* A, const uint16_t* B,
