@@ -89,13 +89,19 @@ def barrier(world):
         dist.barrier()
 
 
-def max_over_ranks(x: float, world: int) -> float:
+def max_over_ranks(x: float, world: int, device: str = "cuda") -> float:
+    """The largest of every rank's x (the slowest rank's time)."""
     if world == 1:
         return x
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    t = torch.tensor([x], dtype=torch.float64, device=device)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def job_throughput(flops_per_rank: float, world: int, ms_slowest: float) -> float:
+    """Whole-job TFLOP/s: all ranks' work over the slowest rank's time."""
+    return world * flops_per_rank / (ms_slowest * 1e-3) / 1e12
 
 
 # ------------------------------------------------------------------ clocks
@@ -162,33 +168,44 @@ class ClockSampler:
 
 # ------------------------------------------------------------------ CPU oracle
 
-def oracle_sample(w: workloads.Workload, budget_s: float):
-    """Times the CPU oracle on a bounded row sample of workload `w`.
+class OracleSampler:
+    """Times the CPU oracle on bounded row samples of workload `w`.
 
-    Returns (TFLOP/s, cores, description). The sample is whole output rows
-    (each row is 2*N*K FLOPs), sized from a one-row probe to take about
-    `budget_s` seconds on every core of this host."""
-    import numpy as np
-    import oracle
+    Inputs are drawn once; the oracle's rate is calibrated once on all cores;
+    each sample is then a set of whole output rows (each row is 2*N*K FLOPs),
+    evenly spread over the output, sized to take about `seconds`."""
 
-    cores = len(os.sched_getaffinity(0))
-    A, B, C = workloads.workload_inputs(w)
-    Ab, Bb = workloads.bf16_bits(A), workloads.bf16_bits(B)
-    Cb = workloads.bf16_bits(C) if C is not None else None
-    probe = np.array([0], dtype=np.int64)
-    t0 = time.perf_counter()
-    oracle.gemm_rows(Ab, Bb, Cb, w.M, w.N, w.K, w.L, w.alpha, w.beta, rows=probe, threads=1)
-    per_row_1core = time.perf_counter() - t0
-    nrows = int(max(cores, min(w.M * w.L, budget_s * cores / max(per_row_1core, 1e-6))))
-    nrows = max(cores, (nrows // cores) * cores)
-    rows = np.linspace(0, w.M * w.L - 1, nrows).astype(np.int64)
-    t0 = time.perf_counter()
-    oracle.gemm_rows(Ab, Bb, Cb, w.M, w.N, w.K, w.L, w.alpha, w.beta, rows=rows, threads=cores)
-    dt = time.perf_counter() - t0
-    flops = 2.0 * nrows * w.N * w.K
-    desc = (f"{nrows} of {w.M * w.L} output rows of {w.name} "
-            f"({flops / 1e9:.1f} GFLOP, {dt:.1f} s, fp64 triple loop)")
-    return flops / dt / 1e12, cores, desc, dt
+    def __init__(self, w: workloads.Workload):
+        import numpy as np
+        self.np = np
+        self.w = w
+        self.cores = len(os.sched_getaffinity(0))
+        A, B, C = workloads.workload_inputs(w)
+        self.Ab, self.Bb = workloads.bf16_bits(A), workloads.bf16_bits(B)
+        self.Cb = workloads.bf16_bits(C) if C is not None else None
+        rows = self.np.arange(self.cores, dtype=self.np.int64)
+        _, dt = self._time(rows)
+        self.rows_per_s = self.cores / max(dt, 1e-6)
+
+    def _time(self, rows):
+        import oracle
+        w = self.w
+        t0 = time.perf_counter()
+        oracle.gemm_rows(self.Ab, self.Bb, self.Cb, w.M, w.N, w.K, w.L, w.alpha, w.beta,
+                         rows=rows, threads=self.cores)
+        return len(rows), time.perf_counter() - t0
+
+    def sample(self, seconds: float):
+        """Returns (TFLOP/s, seconds, description) of one timed sample."""
+        w = self.w
+        n = int(min(w.M * w.L, max(self.cores, seconds * self.rows_per_s)))
+        n = max(self.cores, (n // self.cores) * self.cores)
+        rows = self.np.linspace(0, w.M * w.L - 1, n).astype(self.np.int64)
+        n, dt = self._time(rows)
+        flops = 2.0 * n * w.N * w.K
+        desc = (f"{n} of {w.M * w.L} output rows of {w.name} "
+                f"({flops / 1e9:.1f} GFLOP, {dt:.2f} s, fp64 triple loop, {self.cores} threads)")
+        return flops / dt / 1e12, dt, desc
 
 
 # ------------------------------------------------------------------ GPU arm
@@ -204,6 +221,107 @@ def time_launches(fn, steps: int, stream) -> float:
     end.record(stream)
     torch.cuda.synchronize()
     return start.elapsed_time(end) / steps
+
+
+def time_e2e_serial(g, w, Ah, Bh, Ch, Ad, Bd, Cd, D, stream, warmup, steps, world):
+    """ms per step of copy-in, GEMM, copy-out, one after another on one stream."""
+    Dh = torch.empty(D.shape, dtype=D.dtype).pin_memory()
+
+    def step():
+        Ad.copy_(Ah, non_blocking=True)
+        Bd.copy_(Bh, non_blocking=True)
+        Cd.copy_(Ch, non_blocking=True)
+        g.run(Ad, Bd, Cd, D, w.alpha, w.beta)
+        Dh.copy_(D, non_blocking=True)
+
+    for _ in range(max(1, warmup)):
+        step()
+    barrier(world)
+    return time_launches(step, steps, stream)
+
+
+def time_e2e_pipelined(g, w, Ah, Bh, Ch, dev, comp, warmup, steps, world):
+    """ms per step with copy-in of step i+1 and copy-out of step i-1 overlapping
+    the GEMM of step i (two device buffer sets, events between the streams)."""
+    bufs = [tuple(torch.empty(t.shape, dtype=t.dtype, device=dev) for t in (Ah, Bh, Ch))
+            + (torch.empty(w.L, w.M, w.N, dtype=torch.bfloat16, device=dev),)
+            for _ in range(2)]
+    Dh = [torch.empty(w.L, w.M, w.N, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    cin, cout = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    ev = {k: [torch.cuda.Event() for _ in range(2)] for k in ("in", "gemm", "out")}
+
+    def step(i):
+        b = i % 2
+        Ad, Bd, Cd, Dd = bufs[b]
+        with torch.cuda.stream(cin):
+            if i >= 2:
+                cin.wait_event(ev["gemm"][b])      # step i-2 no longer reads buffer set b
+            Ad.copy_(Ah, non_blocking=True)
+            Bd.copy_(Bh, non_blocking=True)
+            Cd.copy_(Ch, non_blocking=True)
+            ev["in"][b].record(cin)
+        comp.wait_event(ev["in"][b])
+        if i >= 2:
+            comp.wait_event(ev["out"][b])          # step i-2's D has been read back
+        g.run(Ad, Bd, Cd, Dd, w.alpha, w.beta, stream=comp)
+        ev["gemm"][b].record(comp)
+        with torch.cuda.stream(cout):
+            cout.wait_event(ev["gemm"][b])
+            Dh[b].copy_(Dd, non_blocking=True)
+            ev["out"][b].record(cout)
+
+    def run(n):
+        cin.wait_stream(comp)
+        cout.wait_stream(comp)
+        for i in range(n):
+            step(i)
+        comp.wait_stream(cin)
+        comp.wait_stream(cout)
+
+    run(max(2, warmup))
+    torch.cuda.synchronize()
+    barrier(world)
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    start.record(comp)
+    run(steps)
+    end.record(comp)
+    torch.cuda.synchronize()
+    return start.elapsed_time(end) / steps
+
+
+def other_workloads(g, dev, stream, steps: int = 30):
+    """Informational figures for the other workloads (not the headline):
+    TFLOP/s of the 4096^3 and ragged batched GEMMs, launch-to-launch latency
+    of the 256^3 GEMM (latency-bound), and the HBM bandwidth of a skinny
+    8192 x 8192 x 64 GEMM (bound by writing D)."""
+    out = {}
+    cases = [(workloads.WORKLOADS["gemm_256x256x256"], "us"),
+             (workloads.WORKLOADS["gemm_4096x4096x4096"], "tflops"),
+             (workloads.WORKLOADS["gemm_batched4_5000x3000x4000_ragged"], "tflops"),
+             (workloads.Workload("gemm_8192x8192x64_skinny", 8192, 8192, 64, 1, ("uniform",),
+                                 None, 1.0, 0.0, seed=6), "gbs")]
+    for w, kind in cases:
+        A, B, C = workloads.workload_inputs(w)
+        Ad, Bd = A.to(dev), B.to(dev)
+        Cd = C.to(dev) if C is not None else None
+        D = torch.empty(w.L, w.M, w.N, dtype=torch.bfloat16, device=dev)
+        step = lambda: g.run(Ad, Bd, Cd, D, w.alpha, w.beta)
+        for _ in range(3):
+            step()
+        ms = time_launches(step, steps, stream)
+        rec = {"ms_per_launch": round(ms, 5)}
+        if kind == "us":
+            rec["us_per_launch"] = round(ms * 1e3, 2)
+        if kind in ("tflops", "us"):
+            rec["tflops"] = round(w.flops / (ms * 1e-3) / 1e12, 2)
+        if kind == "gbs":
+            rec["gbs"] = round(w.algorithmic_bytes() / (ms * 1e-3) / 1e9, 1)
+            rec["algorithmic_bytes"] = w.algorithmic_bytes()
+        out[w.name] = rec
+        del A, B, C, Ad, Bd, Cd, D
+    torch.cuda.empty_cache()
+    return out
 
 
 def run_ours(args, rank, world, local):
@@ -233,32 +351,29 @@ def run_ours(args, rank, world, local):
     if status != gemm_ws.OK:
         raise RuntimeError(f"device status after timing: {gemm_ws.status_string(status)}")
     tflops_rank = w.flops / (ms * 1e-3) / 1e12
-    value = world * w.flops / (ms * 1e-3) / 1e12
+    value = job_throughput(w.flops, world, ms)
 
-    # End to end through the C ABI with host buffers: pinned host inputs are
-    # copied in and D is read back inside every timed step.
+    # End to end through the C ABI with host buffers: every step copies its
+    # inputs A, B, C in from pinned host memory and reads D back. The timed
+    # loop is a 2-deep software pipeline (two device buffer sets, a copy-in
+    # stream, the compute stream and a copy-out stream), so step i+1's copy-in
+    # and step i-1's copy-out overlap step i's GEMM; all copies of all timed
+    # steps are inside the timed region. The plain serial loop is reported too.
     Ah, Bh, Ch = A.pin_memory(), B.pin_memory(), C.pin_memory()
-    Dh = torch.empty(D.shape, dtype=D.dtype).pin_memory()
-
-    def e2e_step():
-        Ad.copy_(Ah, non_blocking=True)
-        Bd.copy_(Bh, non_blocking=True)
-        Cd.copy_(Ch, non_blocking=True)
-        g.run(Ad, Bd, Cd, D, w.alpha, w.beta)
-        Dh.copy_(D, non_blocking=True)
-
-    for _ in range(max(1, args.warmup)):
-        e2e_step()
     e2e_steps = max(3, min(args.steps, 20))
-    barrier(world)
-    e2e_ms = max_over_ranks(time_launches(e2e_step, e2e_steps, stream), world)
     h2d = sum(t.numel() * t.element_size() for t in (Ah, Bh, Ch))
-    d2h = Dh.numel() * Dh.element_size()
+    d2h = 2 * w.L * w.M * w.N
+    e2e_serial_ms = max_over_ranks(time_e2e_serial(g, w, Ah, Bh, Ch, Ad, Bd, Cd, D, stream,
+                                                   args.warmup, e2e_steps, world), world)
+    del Ad, Bd, Cd, D
+    torch.cuda.empty_cache()
+    e2e_ms = max_over_ranks(time_e2e_pipelined(g, w, Ah, Bh, Ch, dev, stream, args.warmup,
+                                               e2e_steps, world), world)
+    del Ah, Bh, Ch
+    torch.cuda.empty_cache()
 
     # Stream-out overhead: same inputs, interleaved plain / stream-out runs.
     so = workloads.WORKLOADS[workloads.STREAMOUT]
-    del Ah, Bh, Ch, Dh, Ad, Bd, Cd, D
-    torch.cuda.empty_cache()
     As, Bs, _ = workloads.workload_inputs(so)
     As, Bs = As.to(dev), Bs.to(dev)
     Ds = torch.empty(so.L, so.M, so.N, dtype=torch.bfloat16, device=dev)
@@ -279,6 +394,9 @@ def run_ours(args, rank, world, local):
     status = g.query_status()
     if status != gemm_ws.OK:
         raise RuntimeError(f"device status after stream-out: {gemm_ws.status_string(status)}")
+    del As, Bs, Ds, staging, flags
+    torch.cuda.empty_cache()
+    others = other_workloads(g, dev, stream)
     g.close()
 
     if rank != 0:
@@ -287,8 +405,10 @@ def run_ours(args, rank, world, local):
     peak = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
     cpu = None
     if not args.no_cpu_baseline:
-        v, cores, desc, _ = oracle_sample(w, args.cpu_budget)
-        cpu = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc}
+        sampler = OracleSampler(w)
+        v, _, desc = sampler.sample(args.cpu_budget)
+        cpu = {"value": v, "unit": UNIT, "cores": sampler.cores, "kind": "oracle",
+               "sample": desc}
     line = {
         "metric": METRIC,
         "value": round(value, 2),
@@ -314,14 +434,20 @@ def run_ours(args, rank, world, local):
                       "plain_tflops": round(so.flops / (mp * 1e-3) / 1e12, 2)},
         "e2e": {"value": round(world * w.flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": UNIT,
                 "ms_per_step": round(e2e_ms, 4),
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "schedule": "2-deep pipeline: copy-in / GEMM / copy-out streams",
+                "serial_value": round(world * w.flops / (e2e_serial_ms * 1e-3) / 1e12, 2),
+                "serial_ms_per_step": round(e2e_serial_ms, 4)},
         "gpu_launches": args.steps,
+        "pct_of_measured_bf16_sustained": round(
+            100.0 * tflops_rank / peaks.get("bf16_tflops_sustained", peak), 2),
         "roofline": {"bound": "tensor", "achieved": round(tflops_rank, 2), "peak": peak,
                      "unit": "TFLOP/s", "frac": round(tflops_rank / peak, 4),
                      "peak_source": f"{peak_src} bf16 burst (cuBLAS 8192^3)",
                      "traffic": traffic_for(w.name),
                      "algorithmic_bytes_per_launch": w.algorithmic_bytes(),
                      "kernel": "gws::gemm_ws_kernel"},
+        "other_workloads": others,
         "clocks": clocks.summary(),
         "cpu_baseline": cpu,
     }
@@ -359,17 +485,19 @@ def run_kernel_only(args, local):
 
 
 def run_reference(args, rank, world, local):
-    """The reference arm: the CPU oracle, timed on this host's cores."""
+    """The reference arm: the CPU oracle as it stands, timed on this host's
+    cores, on bounded row samples of the headline workload; the whole run
+    (W warm-up + K timed samples) takes about --cpu-budget seconds."""
     if rank != 0:
         return
     w = workloads.WORKLOADS[workloads.HEADLINE]
-    per_step = max(1.0, args.cpu_budget / max(1, args.steps + args.warmup))
+    sampler = OracleSampler(w)
+    per_step = args.cpu_budget / max(1, args.steps + args.warmup)
     for _ in range(args.warmup):
-        oracle_sample(w, per_step)
-    vals, secs = [], 0.0
-    desc, cores = "", 0
+        sampler.sample(per_step)
+    vals, secs, desc = [], 0.0, ""
     for _ in range(args.steps):
-        v, cores, desc, dt = oracle_sample(w, per_step)
+        v, dt, desc = sampler.sample(per_step)
         vals.append(v)
         secs += dt
     value = statistics.median(vals)
@@ -389,8 +517,8 @@ def run_reference(args, rank, world, local):
         "data": "synthetic (seeded uniform/normal bf16, no dataset)",
         "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "L": w.L,
                    "alpha": w.alpha, "beta": w.beta},
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
-                         "sample": desc},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": sampler.cores, "kind": "oracle",
+                         "sample": f"per step: {desc}"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -403,7 +531,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-budget", type=float, default=15.0,
-                    help="seconds of CPU oracle work for the baseline sample")
+                    help="seconds of CPU oracle work: the baseline sample, or the whole "
+                         "reference arm")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--overhead-reps", type=int, default=30)
     ap.add_argument("--kernel-only", action="store_true",
