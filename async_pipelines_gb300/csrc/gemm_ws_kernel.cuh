@@ -65,7 +65,8 @@ constexpr int BK = 64;                   // k-block: 64 bf16 = one 128-byte swiz
 constexpr int UMMA_K = 16;               // K of one tcgen05.mma kind::f16
 constexpr int ACC_BUFS = 2;              // TMEM accumulators (MMA overlaps epilogue)
 constexpr int EPI_N = 32;                // columns per epilogue subtile
-constexpr int EPI_SLOTS = 2;             // D shared-memory slots (store pipeline depth)
+constexpr int EPI_SLOTS = 2;             // D shared-memory slots when C is read
+constexpr int EPI_SLOTS_NOC = 4;         // ... when it is not (the C buffers become D slots)
 constexpr int C_BUFS = 2;                // C shared-memory buffers per epilogue warp
 constexpr int NUM_EPI_WARPS = 4;
 constexpr int STAGING = 128;             // stream-out tile edge
@@ -90,8 +91,8 @@ constexpr int BAR_ACC_FULL = BAR_EMPTY + NUM_STAGES_MAX;
 constexpr int BAR_ACC_EMPTY = BAR_ACC_FULL + ACC_BUFS;
 constexpr int BAR_C_FULL = BAR_ACC_EMPTY + ACC_BUFS;          // [warp quarter][buf]
 constexpr int BAR_D_FULL = BAR_C_FULL + NUM_EPI_WARPS * C_BUFS;
-constexpr int BAR_D_EMPTY = BAR_D_FULL + EPI_SLOTS;
-constexpr int BAR_MMA_DRAIN = BAR_D_EMPTY + EPI_SLOTS;
+constexpr int BAR_D_EMPTY = BAR_D_FULL + EPI_SLOTS_NOC;
+constexpr int BAR_MMA_DRAIN = BAR_D_EMPTY + EPI_SLOTS_NOC;
 constexpr int NUM_BARS = BAR_MMA_DRAIN + 1;
 
 template <int CG>
@@ -113,9 +114,12 @@ struct Cfg {
   // Shared-memory carve-out (offsets from a 1024-byte aligned base).
   static constexpr uint32_t OFF_A = 0;
   static constexpr uint32_t OFF_B = OFF_A + STAGES * A_BYTES;
+  // Epilogue region: D slots 0-1, then either the C buffers (beta != 0) or
+  // D slots 2-3 (beta == 0); slot s sits at OFF_D + s * EPI_SLOT_BYTES.
   static constexpr uint32_t OFF_D = OFF_B + STAGES * B_STAGE_BYTES;
   static constexpr uint32_t OFF_C = OFF_D + EPI_SLOTS * EPI_SLOT_BYTES;
   static constexpr uint32_t OFF_BAR = OFF_C + C_BUFS * EPI_SLOT_BYTES;
+  static_assert(EPI_SLOTS_NOC * EPI_SLOT_BYTES == OFF_BAR - OFF_D, "epilogue region");
   static constexpr uint32_t OFF_TMEM_SLOT = OFF_BAR + NUM_BARS * 8;
   static constexpr uint32_t OFF_ABORT = OFF_TMEM_SLOT + 4;
   static constexpr uint32_t SMEM_USED = OFF_ABORT + 4;
@@ -484,6 +488,7 @@ __device__ __forceinline__ void epilogue_role(const Params& p, uint32_t sbase, u
   const uint32_t row_off = lane * 64;
   const uint32_t swz = (lane >> 1) & 3;
   const int cluster = blockIdx.x / CG, clusters = gridDim.x / CG;
+  const uint32_t nslots = p.has_c ? EPI_SLOTS : EPI_SLOTS_NOC;   // store pipeline depth
   uint32_t u = 0;        // subtiles stored by this warp (D slot ring position)
   uint32_t cu = 0;       // C subtiles consumed by this warp (C ring position)
   uint32_t c_issued = 0; // C subtile loads issued by this warp
@@ -566,12 +571,17 @@ __device__ __forceinline__ void epilogue_role(const Params& p, uint32_t sbase, u
         ++cu;
       }
 
-      // Reuse slot u % EPI_SLOTS only when (a) this warp's TMA store from it
+      // Reuse slot u % nslots only when (a) this warp's TMA store from it
       // has finished reading it and (b) the stream-out consumer released it.
-      const uint32_t slot = u % EPI_SLOTS;
-      if (lane == 0) bulk_wait_read<EPI_SLOTS - 1>();
+      const uint32_t slot = u % nslots;
+      if (lane == 0) {
+        if (nslots == EPI_SLOTS_NOC)
+          bulk_wait_read<EPI_SLOTS_NOC - 1>();
+        else
+          bulk_wait_read<EPI_SLOTS - 1>();
+      }
       if (p.streamout) {
-        if (!warp_wait_spin(bar(BAR_D_EMPTY + slot), ((u / EPI_SLOTS) & 1) ^ 1, wd)) {
+        if (!warp_wait_spin(bar(BAR_D_EMPTY + slot), ((u / nslots) & 1) ^ 1, wd)) {
           ok = false;
           break;
         }
@@ -635,6 +645,7 @@ __device__ __forceinline__ void consumer_role(const Params& p, uint32_t sbase, u
 #ifdef GEMM_WS_DEBUG
   if (p.debug_fault == 1) return;   // injected fault: no tile is ever taken
 #endif
+  const uint32_t nslots = p.has_c ? EPI_SLOTS : EPI_SLOTS_NOC;
   uint32_t u = 0;
   for (int t = cluster; t < p.num_units; t += clusters) {
     const Unit w = unit_coords(p, t);
@@ -645,8 +656,8 @@ __device__ __forceinline__ void consumer_role(const Params& p, uint32_t sbase, u
           (w.l * p.staging_tiles_m + row_tile) * p.staging_tiles_n + w.n0 / STAGING + st;
       uint32_t seq = 0;
       for (int jj = 0; jj < SUB_PER_STAGING; ++jj) {
-        const uint32_t slot = u % EPI_SLOTS;
-        if (!wait_spin<false>(bar(BAR_D_FULL + slot), (u / EPI_SLOTS) & 1, wd)) goto done;
+        const uint32_t slot = u % nslots;
+        if (!wait_spin<false>(bar(BAR_D_FULL + slot), (u / nslots) & 1, wd)) goto done;
         if (jj == 0) seq = atomicAdd(p.counter, 1u);   // completion order
         tma_store_3d(&p.tmS, sbase + C::OFF_D + slot * EPI_SLOT_BYTES, jj * EPI_N, 0,
                      static_cast<int>(seq));
@@ -698,7 +709,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_ws_kernel(const __grid_co
       mbar_init(bar(BAR_ACC_EMPTY + b), NUM_EPI_WARPS * CG);
     }
     for (int i = 0; i < NUM_EPI_WARPS * C_BUFS; ++i) mbar_init(bar(BAR_C_FULL + i), 1);
-    for (int s = 0; s < EPI_SLOTS; ++s) {
+    for (int s = 0; s < EPI_SLOTS_NOC; ++s) {
       mbar_init(bar(BAR_D_FULL + s), NUM_EPI_WARPS);
       mbar_init(bar(BAR_D_EMPTY + s), 1);
     }
