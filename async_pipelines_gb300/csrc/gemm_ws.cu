@@ -21,6 +21,8 @@ struct gemm_ws {
   int device;
   int num_sms;
   int cta_group;                  // 2: CTA-pair tiles (default); 1: single-CTA tiles
+  int multicast;                  // 2: two CTA pairs per cluster share B by TMA multicast
+  int max_quad_clusters;          // co-resident 4-CTA clusters of the multicast kernel
   int group_m;                    // raster group: m-tiles walked per n step
   int max_pair_clusters;          // co-resident 2-CTA clusters of the pair kernel
   uint32_t* work;                 // [0], [2] stream-out counters, [1] status word
@@ -115,32 +117,50 @@ int64_t choose_num_full(int64_t tiles, int64_t P) {
   return best_full;
 }
 
-// Sets the shared-memory attribute of both kernel instances on the current
-// device and returns how many 2-CTA clusters of the pair kernel fit at once.
-cudaError_t configure_kernels(int num_sms, int* max_pair_clusters) {
-  cudaError_t e = cudaFuncSetAttribute(gws::gemm_ws_kernel<1>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(gws::Cfg<1>::SMEM_BYTES));
-  if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(gws::gemm_ws_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(gws::Cfg<2>::SMEM_BYTES));
-  if (e != cudaSuccess) return e;
+// Co-resident clusters of `cs` CTAs of kernel `fn` on the current device.
+template <typename F>
+cudaError_t max_clusters(F fn, int cs, int num_sms, uint32_t smem, int* out) {
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.x = cs;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
-  cfg.gridDim = dim3(2 * (num_sms / 2), 1, 1);
+  cfg.gridDim = dim3(cs * (num_sms / cs), 1, 1);
   cfg.blockDim = dim3(gws::NUM_THREADS, 1, 1);
-  cfg.dynamicSmemBytes = gws::Cfg<2>::SMEM_BYTES;
+  cfg.dynamicSmemBytes = smem;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  int clusters = 0;
-  e = cudaOccupancyMaxActiveClusters(&clusters, gws::gemm_ws_kernel<2>, &cfg);
-  if (e != cudaSuccess) return e;
-  *max_pair_clusters = clusters;
-  return cudaSuccess;
+  return cudaOccupancyMaxActiveClusters(out, fn, &cfg);
+}
+
+// Sets the shared-memory attribute of every kernel instance on the current
+// device and returns how many 2-CTA and 4-CTA clusters fit at once.
+cudaError_t configure_kernels(int num_sms, int* max_pair_clusters, int* max_quad_clusters) {
+  cudaError_t e = cudaFuncSetAttribute(gws::gemm_ws_kernel<1, 1>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(gws::Cfg<1, 1>::SMEM_BYTES));
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(gws::gemm_ws_kernel<2, 1>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(gws::Cfg<2, 1>::SMEM_BYTES));
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(gws::gemm_ws_kernel<2, 2>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(gws::Cfg<2, 2>::SMEM_BYTES));
+  if (e == cudaSuccess)
+    e = max_clusters(gws::gemm_ws_kernel<2, 1>, 2, num_sms, gws::Cfg<2, 1>::SMEM_BYTES,
+                     max_pair_clusters);
+  if (e == cudaSuccess)
+    e = max_clusters(gws::gemm_ws_kernel<2, 2>, 4, num_sms, gws::Cfg<2, 2>::SMEM_BYTES,
+                     max_quad_clusters);
+  return e;
+}
+
+// Persistent clusters the launch may use: SMs for single CTAs, else the
+// co-resident clusters of the kernel's cluster size.
+int64_t cluster_capacity(const gemm_ws* h, int cs) {
+  return cs == 1 ? h->num_sms : (cs == 2 ? h->max_pair_clusters : h->max_quad_clusters);
 }
 
 int launch(gemm_ws* h, const uint16_t* A, const uint16_t* B, const uint16_t* C, uint16_t* D,
@@ -149,7 +169,9 @@ int launch(gemm_ws* h, const uint16_t* A, const uint16_t* B, const uint16_t* C, 
   gws::Params p;
   std::memset(&p, 0, sizeof p);
   const int cg = h->cta_group;
-  const int64_t tiles_m = (M + gws::BM * cg - 1) / (gws::BM * cg);
+  const int mc = cg == 2 ? h->multicast : 1;
+  const int cs = cg * mc;   // CTAs per cluster
+  const int64_t tiles_m = (M + gws::BM * cs - 1) / (gws::BM * cs);
   const int64_t tiles_n = (N + gws::BN - 1) / gws::BN;
   const int64_t num_tiles = L * tiles_m * tiles_n;
   if (num_tiles > kMaxDim) return GEMM_WS_ERR_INVALID_ARG;
@@ -162,10 +184,10 @@ int launch(gemm_ws* h, const uint16_t* A, const uint16_t* B, const uint16_t* C, 
     r = encode3d(h, &p.tmA, A, K, M, L, gws::BK, gws::BM, CU_TENSOR_MAP_SWIZZLE_128B,
                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
     if (r == CUDA_SUCCESS)
-      r = encode3d(h, &p.tmB, B, K, N, L, gws::BK, gws::BN / cg, CU_TENSOR_MAP_SWIZZLE_128B,
+      r = encode3d(h, &p.tmB, B, K, N, L, gws::BK, gws::BN / cs, CU_TENSOR_MAP_SWIZZLE_128B,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
     if (r == CUDA_SUCCESS)
-      r = encode3d(h, &p.tmB2, B, K, N, L, gws::BK, gws::BN / 2 / cg,
+      r = encode3d(h, &p.tmB2, B, K, N, L, gws::BK, gws::BN / 2 / cs,
                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
   }
   if (r == CUDA_SUCCESS && beta != 0.0f)
@@ -190,7 +212,7 @@ int launch(gemm_ws* h, const uint16_t* A, const uint16_t* B, const uint16_t* C, 
   p.tiles_m = static_cast<int>(tiles_m);
   p.tiles_n = static_cast<int>(tiles_n);
   p.num_tiles = static_cast<int>(num_tiles);
-  const int64_t P = cg == 1 ? h->num_sms : h->max_pair_clusters;
+  const int64_t P = cluster_capacity(h, cs);
   const int64_t num_full = choose_num_full(num_tiles, P);
   const int64_t num_units = num_full + 2 * (num_tiles - num_full);
   if (num_units > kMaxDim) return GEMM_WS_ERR_INVALID_ARG;
@@ -217,27 +239,41 @@ int launch(gemm_ws* h, const uint16_t* A, const uint16_t* B, const uint16_t* C, 
   cudaError_t e;
   if (cg == 1) {
     const int grid = static_cast<int>(num_units < h->num_sms ? num_units : h->num_sms);
-    gws::gemm_ws_kernel<1><<<grid, gws::NUM_THREADS, gws::Cfg<1>::SMEM_BYTES, stream>>>(p);
+    gws::gemm_ws_kernel<1, 1><<<grid, gws::NUM_THREADS, gws::Cfg<1, 1>::SMEM_BYTES, stream>>>(p);
     e = cudaGetLastError();
   } else {
-    const int64_t clusters = num_units < h->max_pair_clusters ? num_units : h->max_pair_clusters;
+    const int64_t clusters = num_units < P ? num_units : P;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.x = cs;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
-    cfg.gridDim = dim3(static_cast<unsigned>(2 * clusters), 1, 1);
+    cfg.gridDim = dim3(static_cast<unsigned>(cs * clusters), 1, 1);
     cfg.blockDim = dim3(gws::NUM_THREADS, 1, 1);
-    cfg.dynamicSmemBytes = gws::Cfg<2>::SMEM_BYTES;
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, gws::gemm_ws_kernel<2>, p);
+    if (mc == 1) {
+      cfg.dynamicSmemBytes = gws::Cfg<2, 1>::SMEM_BYTES;
+      e = cudaLaunchKernelEx(&cfg, gws::gemm_ws_kernel<2, 1>, p);
+    } else {
+      cfg.dynamicSmemBytes = gws::Cfg<2, 2>::SMEM_BYTES;
+      e = cudaLaunchKernelEx(&cfg, gws::gemm_ws_kernel<2, 2>, p);
+    }
   }
   if (e != cudaSuccess) return cuda_fail(h, e);
   if (staging) h->counter_parity ^= 1u;   // this launch zeroed the other counter
   return GEMM_WS_OK;
+}
+
+// GEMM_WS_MULTICAST=1 makes two CTA pairs share B by TMA multicast (4-CTA
+// clusters); the default keeps one CTA pair per cluster.
+int multicast_from_env() {
+  if (const char* s = std::getenv("GEMM_WS_MULTICAST")) {
+    if (std::atoi(s) == 1) return 2;
+  }
+  return 1;
 }
 
 // GEMM_WS_CTA_GROUP=1 selects single-CTA 128 x 256 tiles; the default is
@@ -311,8 +347,10 @@ int gemm_ws_create(gemm_ws_t** out, int device) {
   h->encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
 
   h->cta_group = cta_group_from_env();
+  h->multicast = multicast_from_env();
   h->group_m = group_m_from_env();
-  e = configure_kernels(h->num_sms, &h->max_pair_clusters);
+  e = configure_kernels(h->num_sms, &h->max_pair_clusters, &h->max_quad_clusters);
+  if (e == cudaSuccess && h->max_quad_clusters < 1) h->multicast = 1;
   if (e == cudaSuccess && h->max_pair_clusters < 1) h->cta_group = 1;
   if (e == cudaSuccess) e = cudaMalloc(&h->work, kWorkWords * sizeof(uint32_t));
   if (e == cudaSuccess) e = cudaMemset(h->work, 0, kWorkWords * sizeof(uint32_t));
@@ -411,13 +449,13 @@ int gemm_ws_debug_launch_shape(gemm_ws_t* h, int64_t M, int64_t N, int64_t L, in
                                int* clusters, int* num_tiles) {
   if (!h || !cta_group || !clusters || !num_tiles || M <= 0 || N <= 0 || L <= 0)
     return GEMM_WS_ERR_INVALID_ARG;
-  const int cg = h->cta_group;
+  const int cs = h->cta_group * (h->cta_group == 2 ? h->multicast : 1);
   const int64_t tiles =
-      L * ((M + gws::BM * cg - 1) / (gws::BM * cg)) * ((N + gws::BN - 1) / gws::BN);
-  const int64_t cap = cg == 1 ? h->num_sms : h->max_pair_clusters;
+      L * ((M + gws::BM * cs - 1) / (gws::BM * cs)) * ((N + gws::BN - 1) / gws::BN);
+  const int64_t cap = cluster_capacity(h, cs);
   const int64_t full = choose_num_full(tiles, cap);
   const int64_t units = full + 2 * (tiles - full);
-  *cta_group = cg;
+  *cta_group = cs;
   *num_tiles = static_cast<int>(units);
   *clusters = static_cast<int>(units < cap ? units : cap);
   return GEMM_WS_OK;
@@ -453,7 +491,9 @@ struct NoAllocDevice {
   uint32_t counter_parity;
   int num_sms;
   int cta_group;
+  int multicast;
   int max_pair_clusters;
+  int max_quad_clusters;
   uint32_t* scratch;   // device address of g_noalloc_scratch on this device
   unsigned long long timeout_ns;
   PFN_cuTensorMapEncodeTiled_v12000 encode;
@@ -494,10 +534,13 @@ int noalloc_setup(int device, NoAllocDevice** out) {
                                          &q) != cudaSuccess ||
         q != cudaDriverEntryPointSuccess || !fn)
       return GEMM_WS_ERR_CUDA;
-    int pair_clusters = 0;
-    if (configure_kernels(sms, &pair_clusters) != cudaSuccess) return GEMM_WS_ERR_CUDA;
+    int pair_clusters = 0, quad_clusters = 0;
+    if (configure_kernels(sms, &pair_clusters, &quad_clusters) != cudaSuccess)
+      return GEMM_WS_ERR_CUDA;
     d.cta_group = pair_clusters >= 1 ? cta_group_from_env() : 1;
+    d.multicast = quad_clusters >= 1 ? multicast_from_env() : 1;
     d.max_pair_clusters = pair_clusters;
+    d.max_quad_clusters = quad_clusters;
     uint32_t* ptr = nullptr;
     // In host code the array's name is only a host-side stand-in; the kernel
     // must be given this device address instead.
@@ -539,6 +582,8 @@ extern "C" int gemm_ws_run_streamout_noalloc(const uint16_t* A, const uint16_t* 
   h.device = device;
   h.num_sms = d->num_sms;
   h.cta_group = d->cta_group;
+  h.multicast = d->multicast;
+  h.max_quad_clusters = d->max_quad_clusters;
   h.group_m = group_m_from_env();
   h.max_pair_clusters = d->max_pair_clusters;
   h.work = d->scratch;

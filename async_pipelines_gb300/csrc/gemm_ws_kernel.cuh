@@ -95,11 +95,16 @@ constexpr int BAR_D_EMPTY = BAR_D_FULL + EPI_SLOTS_NOC;
 constexpr int BAR_MMA_DRAIN = BAR_D_EMPTY + EPI_SLOTS_NOC;
 constexpr int NUM_BARS = BAR_MMA_DRAIN + 1;
 
-template <int CG>
+template <int CG, int MC>
 struct Cfg {
   static_assert(CG == 1 || CG == 2, "CTA group of 1 or 2");
+  static_assert(MC == 1 || (MC == 2 && CG == 2), "B multicast across two CTA pairs only");
+  static constexpr int CS = CG * MC;                     // CTAs per cluster
   static constexpr int TILE_M = BM * CG;                 // rows per (pair) tile
-  static constexpr int B_ROWS = BN / CG;                 // B rows each CTA loads
+  static constexpr int CLUSTER_M = TILE_M * MC;          // rows per cluster tile
+  static constexpr int B_ROWS = BN / CG;                 // B rows in each CTA's stage
+  static constexpr int B_LOAD_ROWS = BN / CS;            // B rows each CTA loads (whole tile)
+  static constexpr uint16_t ALL_CTAS = static_cast<uint16_t>((1u << CS) - 1u);
   // 64-deep k-blocks per ring stage. The CTA pair takes two (a 128-deep
   // stage of 64 KiB, 3 stages): half the barrier round trips per MMA, which
   // measured ~10 % more tensor throughput per clock than 6 stages of 64.
@@ -327,13 +332,13 @@ __device__ __forceinline__ bool warp_wait_spin(uint32_t bar, uint32_t parity,
 
 // ------------------------------------------------------------ producer
 
-template <int CG>
+template <int CG, int MC>
 __device__ __forceinline__ void producer_role(const Params& p, uint32_t sbase, uint32_t rank,
                                               const Watchdog& wd) {
-  using C = Cfg<CG>;
+  using C = Cfg<CG, MC>;
   auto full = [&](uint32_t s) { return sbase + C::OFF_BAR + 8 * (BAR_FULL + s); };
   auto empty = [&](uint32_t s) { return sbase + C::OFF_BAR + 8 * (BAR_EMPTY + s); };
-  const int cluster = blockIdx.x / CG, clusters = gridDim.x / CG;
+  const int cluster = blockIdx.x / C::CS, clusters = gridDim.x / C::CS;
   uint32_t g = 0;   // k-blocks issued by this CTA so far (ring position)
   bool ok = true;
   // The producer starts in the opposite phase: the first STAGES waits on a
@@ -342,8 +347,14 @@ __device__ __forceinline__ void producer_role(const Params& p, uint32_t sbase, u
   for (int t = cluster; ok && t < p.num_units; t += clusters) {
     const Unit w = unit_coords(p, t);
     const int l = w.l;
-    const int a_row = w.mb * C::TILE_M + static_cast<int>(rank) * BM;
-    const int b_row = w.n0 + static_cast<int>(rank) * (w.width / CG);
+    const int a_row = (w.mb * C::CS + static_cast<int>(rank)) * BM;   // this CTA's rows
+    const int h = static_cast<int>(rank) % CG, pair = static_cast<int>(rank) / CG;
+    // B rows of this CTA's half of the pair's N; with multicast (MC == 2) each
+    // CTA loads the pair-th quarter of that half and sends it to the CTA with
+    // the same half in every pair, at the same shared-memory offset.
+    const int b_rows = w.width / C::CS;
+    const int b_row = w.n0 + h * (w.width / CG) + pair * b_rows;
+    const uint32_t b_off = static_cast<uint32_t>(pair * b_rows) * (BK * 2);
     const bool whole = w.width == BN;
     const CUtensorMap* tmb = whole ? &p.tmB : &p.tmB2;
     const uint32_t tx = whole ? C::STAGE_TX : C::STAGE_TX_HALF;
@@ -351,7 +362,7 @@ __device__ __forceinline__ void producer_role(const Params& p, uint32_t sbase, u
     for (int kb = 0; kb < num_stages; ++kb) {
       const uint32_t s = g % C::STAGES;
       const uint32_t ph = (g / C::STAGES) & 1;
-      if (!token && !wait_spin<false>(empty(s), ph ^ 1, wd)) {
+      if (!token && !wait_spin<MC == 2>(empty(s), ph ^ 1, wd)) {
         ok = false;
         break;
       }
@@ -363,23 +374,27 @@ __device__ __forceinline__ void producer_role(const Params& p, uint32_t sbase, u
         tma_load_3d(sbase + C::OFF_A + s * C::A_BYTES, &p.tmA, full(s), kb * BK, a_row, l);
         tma_load_3d(sbase + C::OFF_B + s * C::B_STAGE_BYTES, tmb, full(s), kb * BK, b_row, l);
       } else {
-        // Both CTAs' copies complete on the even CTA's full[s]; it arms the
-        // barrier for the bytes of both.
-        if (rank == 0) mbar_arrive_expect_tx(full(s), tx);
+        // Both CTAs' copies complete on the pair's even CTA's full[s]; it arms
+        // the barrier for the bytes that land in both of them.
+        if (h == 0) mbar_arrive_expect_tx(full(s), tx);
         // Slabs past K (a ragged last stage) are zero-filled by the TMA.
-        const uint32_t leader_full = mapa_shared(full(s), 0);
+        const uint32_t leader_full = mapa_shared(full(s), static_cast<uint32_t>(pair * CG));
 #pragma unroll
         for (int ks = 0; ks < C::KSUB; ++ks) {
           const int k0 = (kb * C::KSUB + ks) * BK;
           tma_load_3d_pair(sbase + C::OFF_A + s * C::A_BYTES + ks * C::A_BLOCK_BYTES, &p.tmA,
                            leader_full, k0, a_row, l);
-          tma_load_3d_pair(sbase + C::OFF_B + s * C::B_STAGE_BYTES + ks * C::B_BLOCK_BYTES, tmb,
-                           leader_full, k0, b_row, l);
+          const uint32_t bdst = sbase + C::OFF_B + s * C::B_STAGE_BYTES + ks * C::B_BLOCK_BYTES;
+          if constexpr (MC == 1)
+            tma_load_3d_pair(bdst, tmb, leader_full, k0, b_row, l);
+          else
+            tma_load_3d_pair_mc(bdst + b_off, tmb, leader_full, k0, b_row, l,
+                                static_cast<uint16_t>((1u << h) | (1u << (CG + h))));
         }
       }
     }
   }
-  if (!ok && rank == 0) {
+  if (!ok && rank % CG == 0) {
     // Abort: wait (bounded) for the copies of the last stages issued, so no
     // TMA write lands after the CTA pair has released its shared memory.
     const uint32_t first = g > C::STAGES ? g - C::STAGES : 0;
@@ -389,18 +404,22 @@ __device__ __forceinline__ void producer_role(const Params& p, uint32_t sbase, u
 
 // ------------------------------------------------------------ MMA issuer
 
-template <int CG>
+template <int CG, int MC>
 __device__ __forceinline__ void mma_role(const Params& p, uint32_t sbase, uint32_t tmem_base,
-                                         const Watchdog& wd) {
-  using C = Cfg<CG>;
+                                         uint32_t rank, const Watchdog& wd) {
+  using C = Cfg<CG, MC>;
   auto bar = [&](int i) { return sbase + C::OFF_BAR + 8 * i; };
-  auto commit = [&](uint32_t b) {
+  // Stage releases go to every CTA of the cluster (with multicast, each
+  // stage's B bytes were written by both pairs' producers); accumulator
+  // commits go to this pair's two CTAs.
+  const uint16_t pair_mask = static_cast<uint16_t>(0x3u << rank);
+  auto commit = [&](uint32_t b, uint16_t mask) {
     if constexpr (CG == 1)
       umma_commit(b);
     else
-      umma_commit_pair(b, 0x3);
+      umma_commit_pair(b, mask);
   };
-  const int cluster = blockIdx.x / CG, clusters = gridDim.x / CG;
+  const int cluster = blockIdx.x / C::CS, clusters = gridDim.x / C::CS;
   uint32_t g = 0;
   int i = 0;
   bool issued = false;
@@ -433,28 +452,26 @@ __device__ __forceinline__ void mma_role(const Params& p, uint32_t sbase, uint32
             umma_bf16_pair(d_tmem, ad, bd, idesc, acc);
         }
         issued = true;
-        commit(bar(BAR_EMPTY + s));   // stage s free (in every CTA) once these finish
+        commit(bar(BAR_EMPTY + s), C::ALL_CTAS);   // stage s free once these finish
         ++g;
       }
     }
     if (p.num_kb > 0) {
-      commit(bar(BAR_ACC_FULL + b));   // accumulator b complete (in every CTA)
+      commit(bar(BAR_ACC_FULL + b), pair_mask);   // accumulator b complete in the pair
     } else {
       // K == 0: no MMA ran; signal the accumulator barriers directly.
       if constexpr (CG == 1)
         mbar_arrive(bar(BAR_ACC_FULL + b));
       else
-        for (int r = 0; r < CG; ++r) mbar_arrive_cluster(mapa_shared(bar(BAR_ACC_FULL + b), r));
+        for (int r = 0; r < CG; ++r)
+          mbar_arrive_cluster(mapa_shared(bar(BAR_ACC_FULL + b), rank + r));
     }
   }
 done:
   if (issued) {
     // Every MMA this thread issued has finished once this arrives; TMEM can
     // then be freed even on the abort path.
-    if constexpr (CG == 1)
-      umma_commit(bar(BAR_MMA_DRAIN));
-    else
-      umma_commit_pair(bar(BAR_MMA_DRAIN), 0x1);
+    commit(bar(BAR_MMA_DRAIN), static_cast<uint16_t>(1u << rank));
     wait_drain(bar(BAR_MMA_DRAIN), 0);
   }
 }
@@ -475,11 +492,11 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
-template <int CG>
+template <int CG, int MC>
 __device__ __forceinline__ void epilogue_role(const Params& p, uint32_t sbase, uint8_t* smem,
                                               uint32_t tmem_base, uint32_t rank, int warp,
                                               const Watchdog& wd) {
-  using C = Cfg<CG>;
+  using C = Cfg<CG, MC>;
   const int lane = threadIdx.x & 31;
   const int q = warp & 3;   // TMEM lane quarter this warp may access = CTA rows 32q..32q+31
   auto bar = [&](int i) { return sbase + C::OFF_BAR + 8 * i; };
@@ -487,7 +504,7 @@ __device__ __forceinline__ void epilogue_role(const Params& p, uint32_t sbase, u
   // stored at chunk c ^ ((r >> 1) & 3); the same pattern TMA uses.
   const uint32_t row_off = lane * 64;
   const uint32_t swz = (lane >> 1) & 3;
-  const int cluster = blockIdx.x / CG, clusters = gridDim.x / CG;
+  const int cluster = blockIdx.x / C::CS, clusters = gridDim.x / C::CS;
   const uint32_t nslots = p.has_c ? EPI_SLOTS : EPI_SLOTS_NOC;   // store pipeline depth
   uint32_t u = 0;        // subtiles stored by this warp (D slot ring position)
   uint32_t cu = 0;       // C subtiles consumed by this warp (C ring position)
@@ -496,7 +513,7 @@ __device__ __forceinline__ void epilogue_role(const Params& p, uint32_t sbase, u
   for (int t = cluster; t < p.num_units; t += clusters, ++i) {
     const Unit w = unit_coords(p, t);
     const int l = w.l;
-    const int row_tile = w.mb * CG + static_cast<int>(rank);   // this CTA's 128-row slab
+    const int row_tile = w.mb * C::CS + static_cast<int>(rank);   // this CTA's 128-row slab
     const int m0 = row_tile * BM + 32 * q, n0 = w.n0;
     const int nsub = staging_in_part(p, row_tile, w) * SUB_PER_STAGING;
     const uint32_t b = i & 1, aph = (i >> 1) & 1;
@@ -517,10 +534,10 @@ __device__ __forceinline__ void epilogue_role(const Params& p, uint32_t sbase, u
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) {
-        if constexpr (CG == 1)
+        if (CG == 1 || rank % CG == 0)
           mbar_arrive(bar(BAR_ACC_EMPTY + b));
         else
-          mbar_arrive_cluster(mapa_shared(bar(BAR_ACC_EMPTY + b), 0));
+          mbar_arrive_cluster(mapa_shared(bar(BAR_ACC_EMPTY + b), rank - rank % CG));
       }
     };
     if (p.has_c && nsub > 0) issue_c(0);
@@ -530,7 +547,7 @@ __device__ __forceinline__ void epilogue_role(const Params& p, uint32_t sbase, u
 #ifdef GEMM_WS_DEBUG
     // stamp 0: this CTA's part of tile t has its accumulator (MMA done)
     if (p.trace && q == (WARP_EPI0 & 3) && lane == 0)
-      p.trace[(static_cast<size_t>(t) * CG + rank) * 2] = global_timer_ns();
+      p.trace[(static_cast<size_t>(t) * C::CS + rank) * 2] = global_timer_ns();
 #endif
     const uint32_t tacc = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + b * BN;
     if (nsub == 0) release_acc();   // this CTA's rows lie outside M
@@ -619,12 +636,12 @@ __device__ __forceinline__ void epilogue_role(const Params& p, uint32_t sbase, u
 
 // ------------------------------------------------------------ stream-out consumer
 
-template <int CG>
+template <int CG, int MC>
 __device__ __forceinline__ void consumer_role(const Params& p, uint32_t sbase, uint32_t rank,
                                               const Watchdog& wd) {
-  using C = Cfg<CG>;
+  using C = Cfg<CG, MC>;
   auto bar = [&](int i) { return sbase + C::OFF_BAR + 8 * i; };
-  const int cluster = blockIdx.x / CG, clusters = gridDim.x / CG;
+  const int cluster = blockIdx.x / C::CS, clusters = gridDim.x / C::CS;
   // Each stream-out tile has exactly one publishing consumer, which clears
   // the tile's flag words before anything else; so no host-side clearing is
   // needed and nothing in this launch can observe a stale ready word. The
@@ -633,7 +650,7 @@ __device__ __forceinline__ void consumer_role(const Params& p, uint32_t sbase, u
   if (blockIdx.x == 0) st_relaxed_gpu(p.counter_next, 0u);
   for (int t = cluster; t < p.num_units; t += clusters) {
     const Unit w = unit_coords(p, t);
-    const int row_tile = w.mb * CG + static_cast<int>(rank);
+    const int row_tile = w.mb * C::CS + static_cast<int>(rank);
     const int nst = staging_in_part(p, row_tile, w);
     for (int st = 0; st < nst; ++st) {
       const int tile_id =
@@ -649,7 +666,7 @@ __device__ __forceinline__ void consumer_role(const Params& p, uint32_t sbase, u
   uint32_t u = 0;
   for (int t = cluster; t < p.num_units; t += clusters) {
     const Unit w = unit_coords(p, t);
-    const int row_tile = w.mb * CG + static_cast<int>(rank);
+    const int row_tile = w.mb * C::CS + static_cast<int>(rank);
     const int nst = staging_in_part(p, row_tile, w);
     for (int st = 0; st < nst; ++st) {
       const int tile_id =
@@ -675,7 +692,7 @@ __device__ __forceinline__ void consumer_role(const Params& p, uint32_t sbase, u
 #ifdef GEMM_WS_DEBUG
     // stamp 1: every stream-out tile of this CTA's part of tile t is published
     if (p.trace && nst > 0)
-      p.trace[(static_cast<size_t>(t) * CG + rank) * 2 + 1] = global_timer_ns();
+      p.trace[(static_cast<size_t>(t) * C::CS + rank) * 2 + 1] = global_timer_ns();
 #endif
   }
 done:
@@ -684,9 +701,9 @@ done:
 
 // ------------------------------------------------------------ kernel
 
-template <int CG>
+template <int CG, int MC>
 __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_ws_kernel(const __grid_constant__ Params p) {
-  using C = Cfg<CG>;
+  using C = Cfg<CG, MC>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
   const uint32_t pad = ((raw + 1023u) & ~1023u) - raw;
@@ -694,7 +711,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_ws_kernel(const __grid_co
   const uint32_t sbase = raw + pad;
   const int warp = __shfl_sync(0xffffffffu, static_cast<int>(threadIdx.x / 32), 0);
   const int lane = threadIdx.x & 31;
-  const uint32_t rank = CG == 1 ? 0u : cluster_ctarank();
+  const uint32_t rank = C::CS == 1 ? 0u : cluster_ctarank();
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + C::OFF_ABORT);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_TMEM_SLOT);
 
@@ -702,7 +719,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_ws_kernel(const __grid_co
     auto bar = [&](int i) { return sbase + C::OFF_BAR + 8 * i; };
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(bar(BAR_FULL + s), 1);
-      mbar_init(bar(BAR_EMPTY + s), 1);
+      mbar_init(bar(BAR_EMPTY + s), MC);   // one MMA commit per CTA pair
     }
     for (int b = 0; b < ACC_BUFS; ++b) {
       mbar_init(bar(BAR_ACC_FULL + b), 1);
@@ -736,19 +753,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_ws_kernel(const __grid_co
   }
   tc_fence_before_sync();
   __syncthreads();
-  if constexpr (CG == 2) cluster_sync();   // peer's barriers initialised before any remote use
+  if constexpr (C::CS > 1) cluster_sync();   // peers' barriers initialised before remote use
   tc_fence_after_sync();
   const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
   const Watchdog wd{abort_flag, p.status, p.timeout_ns};
 
   if (warp == WARP_TMA) {
-    if (lane == 0) producer_role<CG>(p, sbase, rank, wd);
+    if (lane == 0) producer_role<CG, MC>(p, sbase, rank, wd);
   } else if (warp == WARP_MMA) {
-    if (lane == 0 && rank == 0) mma_role<CG>(p, sbase, tmem_base, wd);
+    if (lane == 0 && rank % CG == 0) mma_role<CG, MC>(p, sbase, tmem_base, rank, wd);
   } else if (warp < WARP_EPI0 + NUM_EPI_WARPS) {
-    epilogue_role<CG>(p, sbase, smem, tmem_base, rank, warp, wd);
+    epilogue_role<CG, MC>(p, sbase, smem, tmem_base, rank, warp, wd);
   } else if (warp == WARP_CONSUMER && p.streamout) {
-    if (lane == 0) consumer_role<CG>(p, sbase, rank, wd);
+    if (lane == 0) consumer_role<CG, MC>(p, sbase, rank, wd);
   }
 
   __syncwarp();
@@ -756,7 +773,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_ws_kernel(const __grid_co
   __syncthreads();
   // The peer may still arrive on, or have the tensor core read, this CTA's
   // shared memory until both CTAs are here.
-  if constexpr (CG == 2) cluster_sync();
+  if constexpr (C::CS > 1) cluster_sync();
   if (warp == WARP_MMA) {
     tc_fence_after_sync();
     if constexpr (CG == 1)

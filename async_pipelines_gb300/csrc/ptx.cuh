@@ -155,6 +155,19 @@ __device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap
       : "memory");
 }
 
+// Pair form with cluster multicast: the box lands at the same shared-memory
+// offset in every CTA of `cta_mask`; each destination's bytes complete on the
+// barrier at `cluster_bar`'s offset in the even CTA of that destination's pair.
+__device__ __forceinline__ void tma_load_3d_pair_mc(uint32_t dst, const CUtensorMap* m,
+                                                    uint32_t cluster_bar, int x, int y, int z,
+                                                    uint16_t cta_mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
+      " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y), "r"(z), "r"(cluster_bar), "h"(cta_mask)
+      : "memory");
+}
+
 // Tiled 3-D TMA store from shared memory; joins this thread's bulk group.
 // Elements outside the tensor's extents are not written.
 __device__ __forceinline__ void tma_store_3d(const CUtensorMap* m, uint32_t src,

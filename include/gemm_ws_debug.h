@@ -27,8 +27,9 @@ extern "C" {
  *  - fault: 0 none; 1 the stream-out consumer warp returns at once, so the
  *    epilogue's wait for a free slot can only end by the watchdog.
  *  - trace: device buffer of num_units * cta_group * 2 uint64 (see
- *    gemm_ws_debug_launch_shape) or NULL. For work unit u and CTA rank r of
- *    its CTA group, trace[(u*cta_group + r)*2] = global time (ns) at which
+ *    gemm_ws_debug_launch_shape; cta_group there is the number of CTAs per
+ *    cluster) or NULL. For work unit u and CTA rank r in its cluster,
+ *    trace[(u*cta_group + r)*2] = global time (ns) at which
  *    that CTA's epilogue saw the unit's accumulator complete, and [...+1] =
  *    time at which its consumer published the last stream-out tile of that
  *    part (written only by gemm_ws_run_streamout; untouched where the part
@@ -36,8 +37,8 @@ extern "C" {
  * Returns GEMM_WS_OK or GEMM_WS_ERR_INVALID_ARG. */
 int gemm_ws_debug_configure(gemm_ws_t* h, int fault, unsigned long long* trace);
 
-/* The launch the handle would make for an M x N x L problem: CTA group size
- * (1 or 2), number of clusters (persistent CTA groups; cluster c takes work
+/* The launch the handle would make for an M x N x L problem: CTAs per
+ * cluster (1, 2, or 4 with B multicast), number of clusters (persistent CTA groups; cluster c takes work
  * units c, c + clusters, ...) and number of work units (whole 256-column
  * tiles, then the last tiles as two 128-column halves). Host arithmetic only. */
 int gemm_ws_debug_launch_shape(gemm_ws_t* h, int64_t M, int64_t N, int64_t L,

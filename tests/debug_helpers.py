@@ -22,15 +22,18 @@ def env(**kv):
                 os.environ[k] = v
 
 
-def debug_handle(cta_group: int = 2, timeout_ms: int = 1000) -> gemm_ws.GemmWS:
+def debug_handle(cta_group: int = 2, timeout_ms: int = 1000,
+                 multicast: int = 0) -> gemm_ws.GemmWS:
     """A handle on the debug build, created with the given tile configuration
-    and per-wait watchdog limit."""
+    (CTA group, B multicast across two CTA pairs) and per-wait watchdog limit."""
     lib = gemm_ws.load_debug_library()
-    with env(GEMM_WS_CTA_GROUP=cta_group, GEMM_WS_TIMEOUT_MS=timeout_ms):
+    with env(GEMM_WS_CTA_GROUP=cta_group, GEMM_WS_TIMEOUT_MS=timeout_ms,
+             GEMM_WS_MULTICAST=multicast):
         return gemm_ws.GemmWS(0, lib=lib)
 
 
 def launch_shape(g: gemm_ws.GemmWS, M: int, N: int, L: int):
+    """(CTAs per cluster, clusters, work units) of the handle's launch."""
     cg, cl, nt = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
     rc = g.lib.gemm_ws_debug_launch_shape(g.handle, M, N, L, ctypes.byref(cg),
                                           ctypes.byref(cl), ctypes.byref(nt))

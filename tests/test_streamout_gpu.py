@@ -29,19 +29,25 @@ def gw():
     g.close()
 
 
-@pytest.fixture(scope="module", params=[2, 1], ids=["cta_pair", "cta_single"])
+@pytest.fixture(scope="module", params=[(2, 0), (1, 0), (2, 1)],
+                ids=["cta_pair", "cta_single", "cta_pair_multicast"])
 def gw_each(request):
-    """A handle per tile configuration: CTA-pair 256x256 tiles (the default)
-    and single-CTA 128x256 tiles (selected at create time by the environment)."""
-    old = os.environ.get("GEMM_WS_CTA_GROUP")
-    os.environ["GEMM_WS_CTA_GROUP"] = str(request.param)
+    """A handle per tile configuration, chosen at create time by the
+    environment: CTA-pair 256x256 tiles (the default), single-CTA 128x256
+    tiles, and CTA pairs sharing B by TMA multicast in 4-CTA clusters."""
+    cg, mc = request.param
+    keys = ("GEMM_WS_CTA_GROUP", "GEMM_WS_MULTICAST")
+    old = {k: os.environ.get(k) for k in keys}
+    os.environ["GEMM_WS_CTA_GROUP"] = str(cg)
+    os.environ["GEMM_WS_MULTICAST"] = str(mc)
     try:
         g = gemm_ws.GemmWS(0)
     finally:
-        if old is None:
-            del os.environ["GEMM_WS_CTA_GROUP"]
-        else:
-            os.environ["GEMM_WS_CTA_GROUP"] = old
+        for k, v in old.items():
+            if v is None:
+                os.environ.pop(k, None)
+            else:
+                os.environ[k] = v
     yield g
     assert g.query_status() == gemm_ws.OK
     g.close()

@@ -23,9 +23,9 @@ from tests.test_streamout_gpu import check_staging
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("cta_group", [2, 1])
-def test_consumer_that_takes_no_tile_times_out_then_recovers(cta_group):
-    g = debug_handle(cta_group=cta_group, timeout_ms=200)
+@pytest.mark.parametrize("cta_group,multicast", [(2, 0), (1, 0), (2, 1)])
+def test_consumer_that_takes_no_tile_times_out_then_recovers(cta_group, multicast):
+    g = debug_handle(cta_group=cta_group, timeout_ms=200, multicast=multicast)
     M, N, K, L = 512, 512, 128, 1
     A, B, _ = workloads.make_inputs(M, N, K, L, ("uniform",), None, seed=41)
     Ad, Bd = A.cuda(), B.cuda()
