@@ -95,9 +95,10 @@ int check_problem(gemm_ws* h, const uint16_t* A, const uint16_t* B, const uint16
 // units so that the persistent schedule's final wave is not half idle.
 // Cluster c runs units c, c + P, ...; a whole tile costs 1, a half ~0.6 (same
 // k-loop and A traffic, half the MMA work). Returns the number of whole
-// tiles; only splits of at most one wave of tiles are considered.
+// tiles; only splits of at most one wave of tiles are considered (with fewer
+// tiles than clusters, splitting spreads a small problem over more SMs).
 int64_t choose_num_full(int64_t tiles, int64_t P) {
-  if (P <= 1 || tiles <= P) return tiles;
+  if (P <= 1) return tiles;
   double best = 0.0;
   int64_t best_full = tiles;
   for (int64_t s = 0; s <= P && s <= tiles; ++s) {

@@ -67,15 +67,15 @@ constexpr int ACC_BUFS = 2;              // TMEM accumulators (MMA overlaps epil
 constexpr int EPI_N = 32;                // columns per epilogue subtile
 constexpr int EPI_SLOTS = 2;             // D shared-memory slots when C is read
 constexpr int EPI_SLOTS_NOC = 4;         // ... when it is not (the C buffers become D slots)
-constexpr int C_BUFS = 2;                // C shared-memory buffers per epilogue warp
-constexpr int NUM_EPI_WARPS = 4;
+constexpr int NUM_EPI_WARPS = 8;         // two per TMEM lane quarter
+constexpr int EPI_HALF_WARPS = 4;        // one per lane quarter: a half covers 128 rows
 constexpr int STAGING = 128;             // stream-out tile edge
 constexpr int SUB_PER_STAGING = STAGING / EPI_N;
 constexpr int WARP_TMA = 0;
 constexpr int WARP_MMA = 1;
 constexpr int WARP_EPI0 = 2;
-constexpr int WARP_CONSUMER = 6;
-constexpr int NUM_THREADS = 7 * 32;
+constexpr int WARP_CONSUMER = WARP_EPI0 + NUM_EPI_WARPS;
+constexpr int NUM_THREADS = (WARP_CONSUMER + 1) * 32;
 constexpr uint32_t TMEM_COLS = ACC_BUFS * BN;   // 512: all of the SM's TMEM
 constexpr uint32_t A_SLAB_BYTES = BM * BK * 2;           // 16 KiB: 128 x 64 slab of A
 constexpr uint32_t EPI_QUARTER_BYTES = 32 * EPI_N * 2;   // 2 KiB: one warp's rows
@@ -89,8 +89,8 @@ constexpr int BAR_FULL = 0;
 constexpr int BAR_EMPTY = BAR_FULL + NUM_STAGES_MAX;
 constexpr int BAR_ACC_FULL = BAR_EMPTY + NUM_STAGES_MAX;
 constexpr int BAR_ACC_EMPTY = BAR_ACC_FULL + ACC_BUFS;
-constexpr int BAR_C_FULL = BAR_ACC_EMPTY + ACC_BUFS;          // [warp quarter][buf]
-constexpr int BAR_D_FULL = BAR_C_FULL + NUM_EPI_WARPS * C_BUFS;
+constexpr int BAR_C_FULL = BAR_ACC_EMPTY + ACC_BUFS;          // [epilogue warp]
+constexpr int BAR_D_FULL = BAR_C_FULL + NUM_EPI_WARPS;
 constexpr int BAR_D_EMPTY = BAR_D_FULL + EPI_SLOTS_NOC;
 constexpr int BAR_MMA_DRAIN = BAR_D_EMPTY + EPI_SLOTS_NOC;
 constexpr int NUM_BARS = BAR_MMA_DRAIN + 1;
@@ -123,7 +123,7 @@ struct Cfg {
   // D slots 2-3 (beta == 0); slot s sits at OFF_D + s * EPI_SLOT_BYTES.
   static constexpr uint32_t OFF_D = OFF_B + STAGES * B_STAGE_BYTES;
   static constexpr uint32_t OFF_C = OFF_D + EPI_SLOTS * EPI_SLOT_BYTES;
-  static constexpr uint32_t OFF_BAR = OFF_C + C_BUFS * EPI_SLOT_BYTES;
+  static constexpr uint32_t OFF_BAR = OFF_C + NUM_EPI_WARPS * EPI_QUARTER_BYTES;
   static_assert(EPI_SLOTS_NOC * EPI_SLOT_BYTES == OFF_BAR - OFF_D, "epilogue region");
   static constexpr uint32_t OFF_TMEM_SLOT = OFF_BAR + NUM_BARS * 8;
   static constexpr uint32_t OFF_ABORT = OFF_TMEM_SLOT + 4;
@@ -498,16 +498,22 @@ __device__ __forceinline__ void epilogue_role(const Params& p, uint32_t sbase, u
                                               const Watchdog& wd) {
   using C = Cfg<CG, MC>;
   const int lane = threadIdx.x & 31;
-  const int q = warp & 3;   // TMEM lane quarter this warp may access = CTA rows 32q..32q+31
+  const int e = warp - WARP_EPI0;    // epilogue warp 0..7
+  const int q = warp & 3;            // TMEM lane quarter it may access = CTA rows 32q..32q+31
+  const int hf = e / EPI_HALF_WARPS; // it takes the unit's subtiles j with j % 2 == hf
   auto bar = [&](int i) { return sbase + C::OFF_BAR + 8 * i; };
   // 64-byte swizzle of a 32-row x 64-byte block: 16-byte chunk c of row r is
   // stored at chunk c ^ ((r >> 1) & 3); the same pattern TMA uses.
   const uint32_t row_off = lane * 64;
   const uint32_t swz = (lane >> 1) & 3;
   const int cluster = blockIdx.x / C::CS, clusters = gridDim.x / C::CS;
-  const uint32_t nslots = p.has_c ? EPI_SLOTS : EPI_SLOTS_NOC;   // store pipeline depth
-  uint32_t u = 0;        // subtiles stored by this warp (D slot ring position)
-  uint32_t cu = 0;       // C subtiles consumed by this warp (C ring position)
+  // Each half of the epilogue warps has its own ring of D slots: one (C is
+  // read, its buffers take the space) or two.
+  const uint32_t per_half = (p.has_c ? EPI_SLOTS : EPI_SLOTS_NOC) / 2;
+  const uint32_t cbuf = sbase + C::OFF_C + static_cast<uint32_t>(e) * EPI_QUARTER_BYTES;
+  const uint32_t cbar = bar(BAR_C_FULL + e);
+  uint32_t u = 0;        // subtiles stored by this warp (slot ring position)
+  uint32_t cu = 0;       // C subtiles consumed by this warp
   uint32_t c_issued = 0; // C subtile loads issued by this warp
   int i = 0;
   for (int t = cluster; t < p.num_units; t += clusters, ++i) {
@@ -515,22 +521,23 @@ __device__ __forceinline__ void epilogue_role(const Params& p, uint32_t sbase, u
     const int l = w.l;
     const int row_tile = w.mb * C::CS + static_cast<int>(rank);   // this CTA's 128-row slab
     const int m0 = row_tile * BM + 32 * q, n0 = w.n0;
-    const int nsub = staging_in_part(p, row_tile, w) * SUB_PER_STAGING;
+    const int nsub = staging_in_part(p, row_tile, w) * SUB_PER_STAGING;   // 0, 4 or 8
     const uint32_t b = i & 1, aph = (i >> 1) & 1;
 
+    // One C buffer per warp: the load for a subtile is issued as soon as the
+    // previous subtile's C has been read out of it.
     auto issue_c = [&](int j) {
-      const uint32_t idx = c_issued++;
+      ++c_issued;
+      __syncwarp();                 // every lane has read the buffer's previous contents
       if (lane == 0) {
-        const uint32_t cb = idx % C_BUFS;
-        const uint32_t cbar = bar(BAR_C_FULL + q * C_BUFS + cb);
-        fence_proxy_async_smem();   // earlier generic reads of this buffer come first
+        fence_proxy_async_smem();   // ... before the TMA (async proxy) overwrites it
         mbar_arrive_expect_tx(cbar, EPI_QUARTER_BYTES);
-        tma_load_3d(sbase + C::OFF_C + cb * EPI_SLOT_BYTES + q * EPI_QUARTER_BYTES, &p.tmC, cbar,
-                    n0 + j * EPI_N, m0, l);
+        tma_load_3d(cbuf, &p.tmC, cbar, n0 + j * EPI_N, m0, l);
       }
     };
     auto release_acc = [&]() {
-      // Accumulator b fully read: hand it back to the MMA warp (even CTA).
+      // Accumulator b fully read by this warp: hand it back to the MMA warp
+      // (the even CTA of the pair).
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) {
@@ -540,65 +547,62 @@ __device__ __forceinline__ void epilogue_role(const Params& p, uint32_t sbase, u
           mbar_arrive_cluster(mapa_shared(bar(BAR_ACC_EMPTY + b), rank - rank % CG));
       }
     };
-    if (p.has_c && nsub > 0) issue_c(0);
+    if (p.has_c && nsub > 0) issue_c(hf);
 
     if (!warp_wait(bar(BAR_ACC_FULL + b), aph, wd)) break;
     tc_fence_after_sync();
 #ifdef GEMM_WS_DEBUG
-    // stamp 0: this CTA's part of tile t has its accumulator (MMA done)
-    if (p.trace && q == (WARP_EPI0 & 3) && lane == 0)
+    // stamp 0: this CTA's part of unit t has its accumulator (MMA done)
+    if (p.trace && q == (WARP_EPI0 & 3) && hf == 0 && lane == 0)
       p.trace[(static_cast<size_t>(t) * C::CS + rank) * 2] = global_timer_ns();
 #endif
     const uint32_t tacc = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + b * BN;
-    if (nsub == 0) release_acc();   // this CTA's rows lie outside M
+    if (nsub == 0) release_acc();   // this CTA's rows lie outside M x N
 
     bool ok = true;
-    for (int j = 0; j < nsub; ++j) {
-      if (p.has_c && j + 1 < nsub) issue_c(j + 1);
-
+    for (int j = hf; j < nsub; j += 2) {
       uint32_t acc[32];
       if (p.num_kb > 0) {
         tmem_ld_32x32b_x32(tacc + j * EPI_N, acc);
         tmem_wait_ld();
       } else {
 #pragma unroll
-        for (int e = 0; e < 32; ++e) acc[e] = 0u;
+        for (int x = 0; x < 32; ++x) acc[x] = 0u;
       }
-      if (j == nsub - 1) release_acc();
+      if (j + 2 >= nsub) release_acc();
 
       float v[32];
 #pragma unroll
-      for (int e = 0; e < 32; ++e) v[e] = p.alpha * __uint_as_float(acc[e]);
+      for (int x = 0; x < 32; ++x) v[x] = p.alpha * __uint_as_float(acc[x]);
       if (p.has_c) {
-        const uint32_t cb = cu % C_BUFS;
-        if (!warp_wait_spin(bar(BAR_C_FULL + q * C_BUFS + cb), (cu / C_BUFS) & 1, wd)) {
+        if (!warp_wait_spin(cbar, cu & 1, wd)) {
           ok = false;
           break;
         }
-        const uint8_t* cbase =
-            smem + C::OFF_C + cb * EPI_SLOT_BYTES + q * EPI_QUARTER_BYTES + row_off;
+        const uint8_t* cq = smem + (cbuf - sbase) + row_off;
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-          const uint4 raw = *reinterpret_cast<const uint4*>(cbase + ((c ^ swz) << 4));
+          const uint4 raw = *reinterpret_cast<const uint4*>(cq + ((c ^ swz) << 4));
           float cf[8];
           unpack_bf16x8(raw, cf);
 #pragma unroll
-          for (int e = 0; e < 8; ++e) v[8 * c + e] = fmaf(p.beta, cf[e], v[8 * c + e]);
+          for (int x = 0; x < 8; ++x) v[8 * c + x] = fmaf(p.beta, cf[x], v[8 * c + x]);
         }
         ++cu;
+        if (j + 2 < nsub) issue_c(j + 2);
       }
 
-      // Reuse slot u % nslots only when (a) this warp's TMA store from it
-      // has finished reading it and (b) the stream-out consumer released it.
-      const uint32_t slot = u % nslots;
+      // Reuse a slot only when (a) this warp's TMA store from it has
+      // finished reading it and (b) the stream-out consumer released it.
+      const uint32_t slot = hf + 2 * (u % per_half);
       if (lane == 0) {
-        if (nslots == EPI_SLOTS_NOC)
-          bulk_wait_read<EPI_SLOTS_NOC - 1>();
+        if (per_half == 2)
+          bulk_wait_read<1>();
         else
-          bulk_wait_read<EPI_SLOTS - 1>();
+          bulk_wait_read<0>();
       }
       if (p.streamout) {
-        if (!warp_wait_spin(bar(BAR_D_EMPTY + slot), ((u / nslots) & 1) ^ 1, wd)) {
+        if (!warp_wait_spin(bar(BAR_D_EMPTY + slot), ((u / per_half) & 1) ^ 1, wd)) {
           ok = false;
           break;
         }
@@ -607,12 +611,12 @@ __device__ __forceinline__ void epilogue_role(const Params& p, uint32_t sbase, u
       uint8_t* dq = smem + C::OFF_D + slot * EPI_SLOT_BYTES + q * EPI_QUARTER_BYTES;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
-        uint4 w;
-        w.x = pack_bf16x2(v[8 * c + 0], v[8 * c + 1]);
-        w.y = pack_bf16x2(v[8 * c + 2], v[8 * c + 3]);
-        w.z = pack_bf16x2(v[8 * c + 4], v[8 * c + 5]);
-        w.w = pack_bf16x2(v[8 * c + 6], v[8 * c + 7]);
-        *reinterpret_cast<uint4*>(dq + row_off + ((c ^ swz) << 4)) = w;
+        uint4 wv;
+        wv.x = pack_bf16x2(v[8 * c + 0], v[8 * c + 1]);
+        wv.y = pack_bf16x2(v[8 * c + 2], v[8 * c + 3]);
+        wv.z = pack_bf16x2(v[8 * c + 4], v[8 * c + 5]);
+        wv.w = pack_bf16x2(v[8 * c + 6], v[8 * c + 7]);
+        *reinterpret_cast<uint4*>(dq + row_off + ((c ^ swz) << 4)) = wv;
       }
       fence_proxy_async_smem();   // generic writes -> visible to the TMA (async proxy)
       __syncwarp();
@@ -626,9 +630,8 @@ __device__ __forceinline__ void epilogue_role(const Params& p, uint32_t sbase, u
     if (!ok) break;
   }
   if (lane == 0) {
-    // C loads still in flight only after an abort: let them land first.
-    for (uint32_t idx = cu; idx < c_issued; ++idx)
-      wait_drain(bar(BAR_C_FULL + q * C_BUFS + idx % C_BUFS), (idx / C_BUFS) & 1);
+    // A C load still in flight only after an abort: let it land first.
+    for (uint32_t idx = cu; idx < c_issued; ++idx) wait_drain(cbar, idx & 1);
     bulk_wait<0>();   // store tail: every D write has landed
   }
   __syncwarp();
@@ -662,8 +665,9 @@ __device__ __forceinline__ void consumer_role(const Params& p, uint32_t sbase, u
 #ifdef GEMM_WS_DEBUG
   if (p.debug_fault == 1) return;   // injected fault: no tile is ever taken
 #endif
-  const uint32_t nslots = p.has_c ? EPI_SLOTS : EPI_SLOTS_NOC;
-  uint32_t u = 0;
+  // Subtile j of a unit sits in the ring of epilogue half j % 2.
+  const uint32_t per_half = (p.has_c ? EPI_SLOTS : EPI_SLOTS_NOC) / 2;
+  uint32_t uh[2] = {0, 0};   // subtiles taken from each half's ring
   for (int t = cluster; t < p.num_units; t += clusters) {
     const Unit w = unit_coords(p, t);
     const int row_tile = w.mb * C::CS + static_cast<int>(rank);
@@ -673,15 +677,16 @@ __device__ __forceinline__ void consumer_role(const Params& p, uint32_t sbase, u
           (w.l * p.staging_tiles_m + row_tile) * p.staging_tiles_n + w.n0 / STAGING + st;
       uint32_t seq = 0;
       for (int jj = 0; jj < SUB_PER_STAGING; ++jj) {
-        const uint32_t slot = u % nslots;
-        if (!wait_spin<false>(bar(BAR_D_FULL + slot), (u / nslots) & 1, wd)) goto done;
+        const int hf = jj & 1;   // SUB_PER_STAGING is even: j % 2 == jj % 2
+        const uint32_t k = uh[hf]++;
+        const uint32_t slot = hf + 2 * (k % per_half);
+        if (!wait_spin<false>(bar(BAR_D_FULL + slot), (k / per_half) & 1, wd)) goto done;
         if (jj == 0) seq = atomicAdd(p.counter, 1u);   // completion order
         tma_store_3d(&p.tmS, sbase + C::OFF_D + slot * EPI_SLOT_BYTES, jj * EPI_N, 0,
                      static_cast<int>(seq));
         bulk_commit();
         bulk_wait_read<0>();                  // slot read: give it back
         mbar_arrive(bar(BAR_D_EMPTY + slot));
-        ++u;
       }
       bulk_wait<0>();                         // staging bytes written
       fence_proxy_async_global();
@@ -725,9 +730,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_ws_kernel(const __grid_co
       mbar_init(bar(BAR_ACC_FULL + b), 1);
       mbar_init(bar(BAR_ACC_EMPTY + b), NUM_EPI_WARPS * CG);
     }
-    for (int i = 0; i < NUM_EPI_WARPS * C_BUFS; ++i) mbar_init(bar(BAR_C_FULL + i), 1);
+    for (int i = 0; i < NUM_EPI_WARPS; ++i) mbar_init(bar(BAR_C_FULL + i), 1);
     for (int s = 0; s < EPI_SLOTS_NOC; ++s) {
-      mbar_init(bar(BAR_D_FULL + s), NUM_EPI_WARPS);
+      mbar_init(bar(BAR_D_FULL + s), EPI_HALF_WARPS);   // the four warps of one half
       mbar_init(bar(BAR_D_EMPTY + s), 1);
     }
     mbar_init(bar(BAR_MMA_DRAIN), 1);

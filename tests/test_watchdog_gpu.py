@@ -26,7 +26,10 @@ pytestmark = pytest.mark.gpu
 @pytest.mark.parametrize("cta_group,multicast", [(2, 0), (1, 0), (2, 1)])
 def test_consumer_that_takes_no_tile_times_out_then_recovers(cta_group, multicast):
     g = debug_handle(cta_group=cta_group, timeout_ms=200, multicast=multicast)
-    M, N, K, L = 512, 512, 128, 1
+    # Several units per cluster, the first a whole 256-column tile: every
+    # epilogue warp needs more shared-memory slots than its ring holds, so it
+    # must wait for the consumer to release one.
+    M, N, K, L = 4096, 4096, 64, 1
     A, B, _ = workloads.make_inputs(M, N, K, L, ("uniform",), None, seed=41)
     Ad, Bd = A.cuda(), B.cuda()
     T = gemm_ws.gemm_ws_streamout_tiles(M, N, L)
