@@ -484,6 +484,41 @@ def run_kernel_only(args, local):
                       "tflops": round(w.flops / (ms * 1e-3) / 1e12, 2)}), flush=True)
 
 
+def run_vs_library(args, local):
+    """Library cross-check (not the product path): the headline GEMM through
+    this library and through torch.addmm (cuBLAS) with the same alpha/beta
+    epilogue, timed in interleaved rounds of --steps launches each on one
+    GPU, so both see the same power and clock state. Prints one JSON line."""
+    from async_pipelines_gb300 import gemm_ws
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream()
+    g = gemm_ws.GemmWS(local)
+    w = workloads.WORKLOADS[workloads.HEADLINE]
+    A, B, C = workloads.workload_inputs(w)
+    Ad, Bd, Cd = A.to(dev), B.to(dev), C.to(dev)
+    D = torch.empty(w.L, w.M, w.N, dtype=torch.bfloat16, device=dev)
+    ours = lambda: g.run(Ad, Bd, Cd, D, w.alpha, w.beta)
+    lib = lambda: torch.addmm(Cd[0], Ad[0], Bd[0].t(), beta=w.beta, alpha=w.alpha, out=D[0])
+    res = {"gemm_ws": [], "torch.addmm": []}
+    for rnd in range(args.rounds):
+        order = [("gemm_ws", ours), ("torch.addmm", lib)]
+        for name, fn in (order if rnd % 2 == 0 else order[::-1]):
+            for _ in range(args.warmup):
+                fn()
+            ms = time_launches(fn, args.steps, stream)
+            res[name].append(w.flops / (ms * 1e-3) / 1e12)
+    status = g.query_status()
+    g.close()
+    if status != gemm_ws.OK:
+        raise RuntimeError(f"device status: {gemm_ws.status_string(status)}")
+    out = {k: {"tflops_median": round(statistics.median(v), 1),
+               "tflops_rounds": [round(x, 1) for x in v]} for k, v in res.items()}
+    print(json.dumps({"workload": w.name, "steps_per_round": args.steps, "rounds": args.rounds,
+                      "interleaved": True, **out}), flush=True)
+
+
 def run_reference(args, rank, world, local):
     """The reference arm: the CPU oracle as it stands, timed on this host's
     cores, on bounded row samples of the headline workload; the whole run
@@ -538,6 +573,10 @@ def main():
     ap.add_argument("--kernel-only", action="store_true",
                     help="launch only the GEMM of --workload (for profilers); no contract line")
     ap.add_argument("--workload", choices=sorted(workloads.WORKLOADS), default=None)
+    ap.add_argument("--vs-library", action="store_true",
+                    help="interleaved rounds against torch.addmm (cuBLAS) on the headline "
+                         "workload; a cross-check, no contract line")
+    ap.add_argument("--rounds", type=int, default=6)
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -547,6 +586,9 @@ def main():
         return
     if args.kernel_only:
         run_kernel_only(args, local)
+        return
+    if args.vs_library:
+        run_vs_library(args, local)
         return
     if world > 1:
         import torch.distributed as dist
