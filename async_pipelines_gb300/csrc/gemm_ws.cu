@@ -17,6 +17,17 @@
 #endif
 #include "gemm_ws_kernel.cuh"
 
+// A tensor map the handle encoded before, and what it describes.
+struct MapCacheEntry {
+  const void* ptr;
+  uint64_t d0, d1, d2;
+  uint32_t b0, b1;
+  int swizzle;
+  bool valid;
+  CUtensorMap map;
+};
+constexpr int kMapCache = 16;
+
 struct gemm_ws {
   int device;
   int num_sms;
@@ -25,11 +36,12 @@ struct gemm_ws {
   int max_quad_clusters;          // co-resident 4-CTA clusters of the multicast kernel
   int group_m;                    // raster group: m-tiles walked per n step
   int max_pair_clusters;          // co-resident 2-CTA clusters of the pair kernel
-  uint32_t* work;                 // [0], [2] stream-out counters, [1] status word
-  uint32_t counter_parity;        // which counter the next stream-out launch uses
+  uint32_t* work;                 // [0] stream-out counter, [1] status, [2] done count
   int last_cuda_error;
   unsigned long long timeout_ns;
   PFN_cuTensorMapEncodeTiled_v12000 encode;
+  MapCacheEntry map_cache[kMapCache];   // recently encoded tensor maps (host memory)
+  int map_cache_next;
 #ifdef GEMM_WS_DEBUG
   int debug_fault;
   unsigned long long* trace;
@@ -40,7 +52,7 @@ namespace {
 
 constexpr int64_t kMaxDim = (int64_t{1} << 31) - 1;
 constexpr int64_t kMaxElems = int64_t{1} << 40;
-constexpr int kWorkWords = 4;   // counters at [0] and [2], status at [1]
+constexpr int kWorkWords = 4;   // counter [0], status [1], consumers done [2]
 
 int cuda_fail(gemm_ws* h, cudaError_t e) {
   if (h) h->last_cuda_error = static_cast<int>(e);
@@ -56,16 +68,40 @@ bool overlaps(const void* a, int64_t abytes, const void* b, int64_t bbytes) {
 }
 
 // A 3-D bf16 tensor {d0 (contiguous), d1, d2}, packed, tiled box {b0, b1, 1}.
+// Encodings are cached per handle (the map depends only on these values), so
+// repeated calls on the same buffers skip the driver's encoder.
 CUresult encode3d(gemm_ws* h, CUtensorMap* m, const void* ptr, uint64_t d0, uint64_t d1,
                   uint64_t d2, uint32_t b0, uint32_t b1, CUtensorMapSwizzle sw,
                   CUtensorMapL2promotion promo) {
+  for (int i = 0; i < kMapCache; ++i) {
+    const MapCacheEntry& e = h->map_cache[i];
+    if (e.valid && e.ptr == ptr && e.d0 == d0 && e.d1 == d1 && e.d2 == d2 && e.b0 == b0 &&
+        e.b1 == b1 && e.swizzle == static_cast<int>(sw)) {
+      std::memcpy(m, &e.map, sizeof(CUtensorMap));
+      return CUDA_SUCCESS;
+    }
+  }
   cuuint64_t dims[3] = {d0, d1, d2};
   cuuint64_t strides[2] = {d0 * 2, d0 * d1 * 2};
   cuuint32_t box[3] = {b0, b1, 1};
   cuuint32_t estr[3] = {1, 1, 1};
-  return h->encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides,
-                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw, promo,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  const CUresult r =
+      h->encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box,
+                estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw, promo, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r == CUDA_SUCCESS) {
+    MapCacheEntry& e = h->map_cache[h->map_cache_next];
+    h->map_cache_next = (h->map_cache_next + 1) % kMapCache;
+    e.ptr = ptr;
+    e.d0 = d0;
+    e.d1 = d1;
+    e.d2 = d2;
+    e.b0 = b0;
+    e.b1 = b1;
+    e.swizzle = static_cast<int>(sw);
+    e.map = *m;
+    e.valid = true;
+  }
+  return r;
 }
 
 int check_problem(gemm_ws* h, const uint16_t* A, const uint16_t* B, const uint16_t* C,
@@ -99,17 +135,15 @@ int check_problem(gemm_ws* h, const uint16_t* A, const uint16_t* B, const uint16
 // tiles than clusters, splitting spreads a small problem over more SMs).
 int64_t choose_num_full(int64_t tiles, int64_t P) {
   if (P <= 1) return tiles;
+  // Cluster c gets ceil-or-floor shares of both the units and the whole
+  // tiles, both non-increasing in c, so cluster 0 is always the slowest.
   double best = 0.0;
   int64_t best_full = tiles;
   for (int64_t s = 0; s <= P && s <= tiles; ++s) {
     const int64_t F = tiles - s, U = F + 2 * s;
-    double worst = 0.0;
-    for (int64_t c = 0; c < P; ++c) {
-      const int64_t n_units = U / P + (c < U % P ? 1 : 0);
-      const int64_t n_full = F / P + (c < F % P ? 1 : 0);
-      const double t = static_cast<double>(n_full) + 0.6 * static_cast<double>(n_units - n_full);
-      if (t > worst) worst = t;
-    }
+    const int64_t n_full = (F + P - 1) / P, n_units = (U + P - 1) / P;
+    const double worst =
+        static_cast<double>(n_full) + 0.6 * static_cast<double>(n_units - n_full);
     if (s == 0 || worst < best - 1e-9) {
       best = worst;
       best_full = F;
@@ -228,9 +262,9 @@ int launch(gemm_ws* h, const uint16_t* A, const uint16_t* B, const uint16_t* C, 
   p.has_c = beta != 0.0f ? 1 : 0;
   p.streamout = staging ? 1 : 0;
   p.flags = flags;
-  p.counter = h->work + (h->counter_parity ? 2 : 0);
-  p.counter_next = h->work + (h->counter_parity ? 0 : 2);
+  p.counter = h->work;
   p.status = h->work + 1;
+  p.done = h->work + 2;
   p.timeout_ns = h->timeout_ns;
 #ifdef GEMM_WS_DEBUG
   p.debug_fault = h->debug_fault;
@@ -264,7 +298,6 @@ int launch(gemm_ws* h, const uint16_t* A, const uint16_t* B, const uint16_t* C, 
     }
   }
   if (e != cudaSuccess) return cuda_fail(h, e);
-  if (staging) h->counter_parity ^= 1u;   // this launch zeroed the other counter
   return GEMM_WS_OK;
 }
 
@@ -489,7 +522,6 @@ constexpr int kNoAllocMaxDevices = 64;
 
 struct NoAllocDevice {
   bool ready;
-  uint32_t counter_parity;
   int num_sms;
   int cta_group;
   int multicast;
@@ -509,8 +541,8 @@ std::mutex g_noalloc_mutex;
 
 }  // namespace
 
-// words 0 and 2: the two alternating stream-out sequence counters (each
-// launch zeroes the one the next launch uses); word 1: watchdog status.
+// word 0: stream-out sequence counter, word 1: watchdog status, word 2:
+// consumer warps finished (the kernel returns words 0 and 2 to zero).
 static __device__ __align__(256) uint32_t g_noalloc_scratch[kNoAllocScratchWords];
 
 namespace {
@@ -577,7 +609,6 @@ extern "C" int gemm_ws_run_streamout_noalloc(const uint16_t* A, const uint16_t* 
   NoAllocDevice* d = nullptr;
   int rc = noalloc_setup(device, &d);
   if (rc != GEMM_WS_OK) return rc;
-  std::lock_guard<std::mutex> lock(g_noalloc_mutex);   // the counter parity is shared
   gemm_ws h;   // a handle on the host stack that borrows the static scratch
   std::memset(&h, 0, sizeof h);
   h.device = device;
@@ -590,8 +621,5 @@ extern "C" int gemm_ws_run_streamout_noalloc(const uint16_t* A, const uint16_t* 
   h.work = d->scratch;
   h.timeout_ns = d->timeout_ns;
   h.encode = d->encode;
-  h.counter_parity = d->counter_parity;
-  rc = gemm_ws_run_streamout(&h, A, B, C, D, M, N, K, L, alpha, beta, staging, flags, stream);
-  d->counter_parity = h.counter_parity;
-  return rc;
+  return gemm_ws_run_streamout(&h, A, B, C, D, M, N, K, L, alpha, beta, staging, flags, stream);
 }

@@ -156,8 +156,9 @@ struct Params {
   int has_c;                     // beta != 0
   int streamout;
   uint32_t* flags;               // 2 * T words (stream-out)
-  uint32_t* counter;             // stream-out sequence counter (zero at launch)
-  uint32_t* counter_next;        // the other counter: zeroed here for the next launch
+  uint32_t* counter;             // stream-out sequence counter (zero at launch; the
+                                 // kernel's last consumer warp zeroes it again)
+  uint32_t* done;                // consumer warps finished (same life cycle)
   uint32_t* status;              // watchdog status word
   unsigned long long timeout_ns; // bound of every single wait
 #ifdef GEMM_WS_DEBUG
@@ -668,10 +669,7 @@ __device__ __forceinline__ void consumer_role(const Params& p, uint32_t sbase, u
   const int cluster = blockIdx.x / C::CS, clusters = gridDim.x / C::CS;
   // Each stream-out tile has exactly one publishing consumer, which clears
   // the tile's flag words before anything else; so no host-side clearing is
-  // needed and nothing in this launch can observe a stale ready word. The
-  // first CTA also zeroes the counter that the NEXT launch will use (stream
-  // order makes that visible to it).
-  if (blockIdx.x == 0) st_relaxed_gpu(p.counter_next, 0u);
+  // needed and nothing in this launch can observe a stale ready word.
   for (int t = cluster; t < p.num_units; t += clusters) {
     const Unit w = unit_coords(p, t);
     const int row_tile = w.mb * C::CS + static_cast<int>(rank);
@@ -683,12 +681,12 @@ __device__ __forceinline__ void consumer_role(const Params& p, uint32_t sbase, u
       st_relaxed_gpu(p.flags + 2 * tile_id + 1, 0u);
     }
   }
-#ifdef GEMM_WS_DEBUG
-  if (p.debug_fault == 1) return;   // injected fault: no tile is ever taken
-#endif
   // Subtile j of a unit sits in the ring of epilogue half j % 2.
   const uint32_t per_half = (p.has_c ? EPI_SLOTS : EPI_SLOTS_NOC) / 2;
   uint32_t uh[2] = {0, 0};   // subtiles taken from each half's ring
+#ifdef GEMM_WS_DEBUG
+  if (p.debug_fault == 1) goto done;   // injected fault: no tile is ever taken
+#endif
   for (int t = cluster; t < p.num_units; t += clusters) {
     const Unit w = unit_coords(p, t);
     const int row_tile = w.mb * C::CS + static_cast<int>(rank);
@@ -723,6 +721,17 @@ __device__ __forceinline__ void consumer_role(const Params& p, uint32_t sbase, u
   }
 done:
   bulk_wait<0>();
+  // The last consumer warp of the launch to get here (every one gets here,
+  // also after an abort) zeroes the sequence counter for the next launch:
+  // all counter updates of this launch happen before the arrivals on `done`.
+  // So a call needs no host-side reset, and a launch replayed from a CUDA
+  // graph starts from zero as well.
+  __threadfence();
+  if (atomicAdd(p.done, 1u) == gridDim.x - 1) {
+    atomicExch(p.counter, 0u);
+    atomicExch(p.done, 0u);
+    __threadfence();
+  }
 }
 
 // ------------------------------------------------------------ kernel

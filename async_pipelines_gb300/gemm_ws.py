@@ -127,6 +127,15 @@ def _ptr(t: Optional[torch.Tensor]):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
 
+def _stream_handle(stream) -> int:
+    """The raw cudaStream_t of `stream` (default: the current torch stream)."""
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
 def _stream(stream) -> ctypes.c_void_p:
     if stream is None:
         stream = torch.cuda.current_stream()
@@ -167,10 +176,13 @@ def gemm_ws_last_cuda_error(h) -> int:
 
 # ------------------------------------------------------------------ tensor API
 
+_BF16 = torch.bfloat16
+
+
 def _check_operands(A, B, C, D):
-    for name, t in (("A", A), ("B", B), ("D", D)) + ((("C", C),) if C is not None else ()):
-        if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
-            raise ValueError(f"{name} must be a contiguous bf16 CUDA tensor")
+    for t in (A, B, D) if C is None else (A, B, C, D):
+        if t.dtype is not _BF16 or not t.is_cuda or not t.is_contiguous():
+            raise ValueError("A, B, C and D must be contiguous bf16 CUDA tensors")
     if A.dim() != 3 or B.dim() != 3 or D.dim() != 3:
         raise ValueError("A (L,M,K), B (L,N,K) and D (L,M,N) must be 3-D")
     L, M, K = A.shape
@@ -218,9 +230,11 @@ class GemmWS:
         A: (L, M, K), B: (L, N, K) (column-major K x N per batch), C/D: (L, M, N).
         """
         M, N, K, L = _check_operands(A, B, C, D)
-        rc = self.lib.gemm_ws_run(self.handle, _ptr(A), _ptr(B), _ptr(C), _ptr(D), M, N, K, L,
-                                  float(alpha), float(beta), _stream(stream))
-        self._raise(rc, "gemm_ws_run")
+        rc = self.lib.gemm_ws_run(self.handle, A.data_ptr(), B.data_ptr(),
+                                  None if C is None else C.data_ptr(), D.data_ptr(), M, N, K, L,
+                                  alpha, beta, _stream_handle(stream))
+        if rc != OK:
+            self._raise(rc, "gemm_ws_run")
         return D
 
     def run_streamout(self, A, B, C, D, staging, flags, alpha=1.0, beta=0.0, stream=None):

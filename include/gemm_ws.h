@@ -25,8 +25,8 @@
  *
  * Ownership: every data pointer is a borrowed DEVICE pointer on the handle's
  * device; the caller owns it and keeps it alive until the stream work ends.
- * The handle owns only its small device workspace (two stream-out counters
- * and a status word).
+ * The handle owns only its small device workspace (the stream-out sequence
+ * counter, a status word, a completion count).
  *
  * Errors: every entry point returns a gemm_ws_status. A call that returns an
  * error other than GEMM_WS_ERR_CUDA launched nothing and wrote nothing. All
@@ -134,11 +134,10 @@ int64_t gemm_ws_streamout_tiles(int64_t M, int64_t N, int64_t L);
  *    checks, kernel attribute, address of the scratch array); make that first
  *    call before any stream capture.
  *  - Every call shares the one scratch array, which keeps the last call's
- *    contents. It holds two sequence counters used alternately: each call's
- *    kernel zeroes the one the next call will use, so consecutive calls on
- *    one stream need no clearing. Calls that overlap on the GPU (e.g. on two
- *    streams) race on the counters and produce wrong sequence numbers:
- *    serialise them.
+ *    contents. The kernel returns its sequence counter to zero before it
+ *    ends, so consecutive calls need no clearing. Calls that overlap on the
+ *    GPU (e.g. on two streams) race on the counter and produce wrong sequence
+ *    numbers: serialise them.
  *  - A watchdog timeout is not reported through a status query here; it shows
  *    as tiles whose ready word flags[2t+1] stayed 0. */
 int gemm_ws_run_streamout_noalloc(const uint16_t* A, const uint16_t* B,
