@@ -33,6 +33,7 @@ struct gemm_ws {
   int num_sms;
   int cta_group;                  // 2: CTA-pair tiles (default); 1: single-CTA tiles
   int multicast;                  // 2: two CTA pairs per cluster share B by TMA multicast
+  int pdl;                        // launch with programmatic stream serialisation
   int max_quad_clusters;          // co-resident 4-CTA clusters of the multicast kernel
   int group_m;                    // raster group: m-tiles walked per n step
   int max_pair_clusters;          // co-resident 2-CTA clusters of the pair kernel
@@ -272,24 +273,35 @@ int launch(gemm_ws* h, const uint16_t* A, const uint16_t* B, const uint16_t* C, 
 #endif
 
   cudaError_t e;
-  if (cg == 1) {
-    const int grid = static_cast<int>(num_units < h->num_sms ? num_units : h->num_sms);
-    gws::gemm_ws_kernel<1, 1><<<grid, gws::NUM_THREADS, gws::Cfg<1, 1>::SMEM_BYTES, stream>>>(p);
-    e = cudaGetLastError();
-  } else {
+  {
+    // Programmatic stream serialisation: this grid may be scheduled while the
+    // previous kernel in the stream finishes; it waits for that kernel before
+    // its first global-memory access (grid_dependency_wait in the kernel).
     const int64_t clusters = num_units < P ? num_units : P;
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = cs;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
+    cudaLaunchAttribute attr[2];
+    int nattr = 0;
+    if (h->pdl) {
+      attr[nattr].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+      attr[nattr].val.programmaticStreamSerializationAllowed = 1;
+      ++nattr;
+    }
+    if (cs > 1) {
+      attr[nattr].id = cudaLaunchAttributeClusterDimension;
+      attr[nattr].val.clusterDim.x = cs;
+      attr[nattr].val.clusterDim.y = 1;
+      attr[nattr].val.clusterDim.z = 1;
+      ++nattr;
+    }
     cfg.gridDim = dim3(static_cast<unsigned>(cs * clusters), 1, 1);
     cfg.blockDim = dim3(gws::NUM_THREADS, 1, 1);
     cfg.stream = stream;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    if (mc == 1) {
+    cfg.numAttrs = nattr;
+    if (cg == 1) {
+      cfg.dynamicSmemBytes = gws::Cfg<1, 1>::SMEM_BYTES;
+      e = cudaLaunchKernelEx(&cfg, gws::gemm_ws_kernel<1, 1>, p);
+    } else if (mc == 1) {
       cfg.dynamicSmemBytes = gws::Cfg<2, 1>::SMEM_BYTES;
       e = cudaLaunchKernelEx(&cfg, gws::gemm_ws_kernel<2, 1>, p);
     } else {
@@ -306,6 +318,14 @@ int launch(gemm_ws* h, const uint16_t* A, const uint16_t* B, const uint16_t* C, 
 int multicast_from_env() {
   if (const char* s = std::getenv("GEMM_WS_MULTICAST")) {
     if (std::atoi(s) == 1) return 2;
+  }
+  return 1;
+}
+
+// GEMM_WS_PDL=0 launches without programmatic dependent launch (default on).
+int pdl_from_env() {
+  if (const char* s = std::getenv("GEMM_WS_PDL")) {
+    if (std::atoi(s) == 0) return 0;
   }
   return 1;
 }
@@ -382,6 +402,7 @@ int gemm_ws_create(gemm_ws_t** out, int device) {
 
   h->cta_group = cta_group_from_env();
   h->multicast = multicast_from_env();
+  h->pdl = pdl_from_env();
   h->group_m = group_m_from_env();
   e = configure_kernels(h->num_sms, &h->max_pair_clusters, &h->max_quad_clusters);
   if (e == cudaSuccess && h->max_quad_clusters < 1) h->multicast = 1;
@@ -615,6 +636,7 @@ extern "C" int gemm_ws_run_streamout_noalloc(const uint16_t* A, const uint16_t* 
   h.num_sms = d->num_sms;
   h.cta_group = d->cta_group;
   h.multicast = d->multicast;
+  h.pdl = pdl_from_env();
   h.max_quad_clusters = d->max_quad_clusters;
   h.group_m = group_m_from_env();
   h.max_pair_clusters = d->max_pair_clusters;

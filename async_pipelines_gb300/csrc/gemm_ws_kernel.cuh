@@ -792,6 +792,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_ws_kernel(const __grid_co
   tc_fence_after_sync();
   const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
   const Watchdog wd{abort_flag, p.status, p.timeout_ns};
+  // Everything above touches only this CTA's shared and tensor memory, so it
+  // may overlap the previous kernel's tail; global memory is touched only
+  // after that kernel has completed. The next launch may be scheduled now
+  // (its CTAs take SMs as this grid's CTAs leave them).
+  grid_dependency_wait();
+  if (threadIdx.x == 0) grid_launch_dependents();
 
   if (warp == WARP_TMA || warp == WARP_TMA_B) {
     if (lane == 0)

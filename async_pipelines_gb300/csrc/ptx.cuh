@@ -116,6 +116,22 @@ __device__ __forceinline__ void cluster_sync() {
                "barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
+// ------------------------------------------------- programmatic dependent launch
+
+// Block until the grids this one depends on (the previous kernel in the
+// stream, when launched with programmatic stream serialisation) have
+// completed and their memory operations are visible; returns at once
+// otherwise.
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Allow the next grid in the stream to be scheduled before this one ends
+// (it still waits in grid_dependency_wait for this grid to complete).
+__device__ __forceinline__ void grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- TMA / bulk
 
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* m) {
