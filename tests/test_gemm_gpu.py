@@ -224,3 +224,61 @@ def test_workload_parity(gw, name):
     d, ref = run_case(gw, w.M, w.N, w.K, w.L, w.alpha, w.beta, ab=w.ab_dist, cd=w.c_dist,
                       seed=w.seed, rows=rows)
     assert_gemm_close(d, ref, w.K, name)
+
+
+# ------------------------------------------------------------------ randomized and guarded
+
+def _random_cases(n, seed):
+    rng = np.random.default_rng(seed)
+    for _ in range(n):
+        M = int(rng.integers(1, 700))
+        N = 8 * int(rng.integers(1, 90))
+        K = 8 * int(rng.integers(0, 80))
+        L = int(rng.integers(1, 4))
+        alpha = float(np.float32(rng.choice([1.0, -0.5, 2.0, 0.75])))
+        beta = float(np.float32(rng.choice([0.0, 0.0, 1.0, -1.5])))
+        yield M, N, K, L, alpha, beta
+
+
+@pytest.mark.parametrize("case", list(_random_cases(16, seed=2024)),
+                         ids=lambda c: "x".join(str(v) for v in c[:4]))
+def test_random_shapes_match_oracle(gw_each, case):
+    """Seeded random problems: ragged M, N, K (including K = 0), batches,
+    alpha/beta signs; every element checked against the oracle."""
+    M, N, K, L, alpha, beta = case
+    cd = ("uniform",) if beta != 0 else None
+    d, ref = run_case(gw_each, M, N, K, L, alpha, beta, ab=("normal", 0.5), cd=cd,
+                      seed=M * 7 + N + K)
+    assert_gemm_close(d, ref, K, f"{M}x{N}x{K}x{L}")
+
+
+def test_d_neighbours_are_never_written(gw_each):
+    """D lives inside a larger buffer; the elements before and after it (and
+    hence outside the ragged M x N edges of the TMA stores) keep their canary
+    values."""
+    M, N, K, L = 333, 264, 72, 2
+    A, B, C = workloads.make_inputs(M, N, K, L, ("uniform",), ("uniform",), seed=90)
+    pad = 4096
+    buf = torch.full((pad + L * M * N + pad,), 123.0, dtype=torch.bfloat16, device="cuda")
+    D = buf[pad:pad + L * M * N].view(L, M, N)
+    gw_each.run(A.cuda(), B.cuda(), C.cuda(), D, 1.0, 1.0)
+    torch.cuda.synchronize()
+    assert torch.all(buf[:pad] == 123.0) and torch.all(buf[pad + L * M * N:] == 123.0)
+    ref = oracle.gemm(bits_of(A), bits_of(B), bits_of(C), M, N, K, L, 1.0, 1.0)
+    assert_gemm_close(bits_of(D), ref, K, "guarded D")
+
+
+def test_create_rejects_a_missing_device():
+    with pytest.raises(gemm_ws.GemmWSError) as e:
+        gemm_ws.GemmWS(torch.cuda.device_count())
+    assert e.value.status == gemm_ws.ERR_INVALID_ARG
+
+
+def test_oversized_dimensions_are_rejected(gw):
+    A = torch.zeros(1, 8, 8, dtype=torch.bfloat16, device="cuda")
+    rc = gemm_ws.gemm_ws_run(gw.handle, A, A, None, A.clone(), 1 << 31, 8, 8, 1, 1.0, 0.0)
+    assert rc == gemm_ws.ERR_INVALID_ARG
+    # L*M*N = 2^42 elements, beyond the 2^40 limit: rejected by the size check,
+    # before any pointer is used (the buffers here are far smaller)
+    rc = gemm_ws.gemm_ws_run(gw.handle, A, A, None, A.clone(), 1 << 21, 1 << 21, 8, 1, 1.0, 0.0)
+    assert rc == gemm_ws.ERR_INVALID_ARG
