@@ -37,7 +37,10 @@ struct gemm_ws {
   int max_quad_clusters;          // co-resident 4-CTA clusters of the multicast kernel
   int group_m;                    // raster group: m-tiles walked per n step
   int max_pair_clusters;          // co-resident 2-CTA clusters of the pair kernel
+  int split_k;                    // allow split-K for few-tile, long-K problems
   uint32_t* work;                 // [0] stream-out counter, [1] status, [2] done count
+  float* partial;                 // split-K partials: num_sms parts of 128 x 256 fp32
+  uint32_t* split_count;          // split-K arrival counters, num_sms * 32 words (kept at zero)
   int last_cuda_error;
   unsigned long long timeout_ns;
   PFN_cuTensorMapEncodeTiled_v12000 encode;
@@ -199,6 +202,68 @@ int64_t cluster_capacity(const gemm_ws* h, int cs) {
   return cs == 1 ? h->num_sms : (cs == 2 ? h->max_pair_clusters : h->max_quad_clusters);
 }
 
+// Split-K is used when the output has at most half as many tiles as the GPU
+// has persistent clusters and K is long: each tile's K range is cut into
+// `ksplit` pieces of at least kMinSplitK elements, run as separate units;
+// for every 32 x 32 chunk, the piece that writes its fp32 partial last sums
+// all of them. Every split unit runs in the first (only) wave, so the
+// workspace needs at most one 128 x 256 fp32 part (and one set of chunk
+// counters) per CTA of the launch.
+constexpr int64_t kMinSplitK = 1024;
+constexpr int64_t kMaxSplit = 32;
+constexpr size_t kPartBytes = size_t{gws::BM} * gws::BN * sizeof(float);
+// One counter per 32 x 32 chunk of a part: 4 lane quarters x 8 subtiles.
+constexpr size_t kCountersPerPart = 4 * gws::SUB_PER_PART;
+
+struct Plan {
+  int cs;              // CTAs per cluster
+  int64_t tiles_m, tiles_n, num_tiles;
+  int64_t num_full;    // whole-width units (the rest of the tiles run as halves)
+  int64_t num_units;
+  int64_t num_stages;  // ring stages covering K
+  int64_t ksplit, split_stages;
+  int64_t clusters;    // persistent clusters launched
+};
+
+// The persistent schedule of one launch: host arithmetic only, shared by the
+// launch and the debug query.
+Plan make_plan(const gemm_ws* h, int64_t M, int64_t N, int64_t K, int64_t L, bool streamout) {
+  Plan q;
+  const int cg = h->cta_group;
+  q.cs = cg * (cg == 2 ? h->multicast : 1);
+  q.tiles_m = (M + gws::BM * q.cs - 1) / (gws::BM * q.cs);
+  q.tiles_n = (N + gws::BN - 1) / gws::BN;
+  q.num_tiles = L * q.tiles_m * q.tiles_n;
+  const int64_t ksub = cg == 1 ? gws::Cfg<1, 1>::KSUB : gws::Cfg<2, 1>::KSUB;
+  q.num_stages = ((K + gws::BK - 1) / gws::BK + ksub - 1) / ksub;
+  const int64_t P = cluster_capacity(h, q.cs);
+  q.ksplit = 1;
+  q.split_stages = q.num_stages;
+  // Stream-out keeps whole tiles: its consumer takes every tile where it is
+  // computed.
+  if (!streamout && h->split_k && h->partial && 2 * q.num_tiles <= P) {
+    int64_t S = P / q.num_tiles;
+    const int64_t by_k = K / kMinSplitK;
+    if (S > by_k) S = by_k;
+    if (S > kMaxSplit) S = kMaxSplit;
+    if (S > q.num_stages) S = q.num_stages;
+    if (S >= 2) {
+      q.split_stages = (q.num_stages + S - 1) / S;
+      q.ksplit = (q.num_stages + q.split_stages - 1) / q.split_stages;   // none empty
+      if (q.ksplit < 2) q.split_stages = q.num_stages, q.ksplit = 1;
+    }
+  }
+  if (q.ksplit > 1) {
+    q.num_full = q.num_tiles;
+    q.num_units = q.num_tiles * q.ksplit;
+  } else {
+    q.num_full = choose_num_full(q.num_tiles, P);
+    q.num_units = q.num_full + 2 * (q.num_tiles - q.num_full);
+  }
+  q.clusters = q.num_units < P ? q.num_units : P;
+  return q;
+}
+
 int launch(gemm_ws* h, const uint16_t* A, const uint16_t* B, const uint16_t* C, uint16_t* D,
            int64_t M, int64_t N, int64_t K, int64_t L, float alpha, float beta,
            uint16_t* staging, uint32_t* flags, cudaStream_t stream) {
@@ -206,11 +271,9 @@ int launch(gemm_ws* h, const uint16_t* A, const uint16_t* B, const uint16_t* C, 
   std::memset(&p, 0, sizeof p);
   const int cg = h->cta_group;
   const int mc = cg == 2 ? h->multicast : 1;
-  const int cs = cg * mc;   // CTAs per cluster
-  const int64_t tiles_m = (M + gws::BM * cs - 1) / (gws::BM * cs);
-  const int64_t tiles_n = (N + gws::BN - 1) / gws::BN;
-  const int64_t num_tiles = L * tiles_m * tiles_n;
-  if (num_tiles > kMaxDim) return GEMM_WS_ERR_INVALID_ARG;
+  const Plan q = make_plan(h, M, N, K, L, staging != nullptr);
+  const int cs = q.cs;   // CTAs per cluster
+  if (q.num_units > kMaxDim) return GEMM_WS_ERR_INVALID_ARG;
   const int64_t stn = (N + gws::STAGING - 1) / gws::STAGING;
   const int64_t T = L * ((M + gws::STAGING - 1) / gws::STAGING) * stn;
   if (T > kMaxDim) return GEMM_WS_ERR_INVALID_ARG;
@@ -245,16 +308,17 @@ int launch(gemm_ws* h, const uint16_t* A, const uint16_t* B, const uint16_t* C, 
   p.N = static_cast<int>(N);
   p.K = static_cast<int>(K);
   p.L = static_cast<int>(L);
-  p.tiles_m = static_cast<int>(tiles_m);
-  p.tiles_n = static_cast<int>(tiles_n);
-  p.num_tiles = static_cast<int>(num_tiles);
-  const int64_t P = cluster_capacity(h, cs);
-  const int64_t num_full = choose_num_full(num_tiles, P);
-  const int64_t num_units = num_full + 2 * (num_tiles - num_full);
-  if (num_units > kMaxDim) return GEMM_WS_ERR_INVALID_ARG;
-  p.num_full = static_cast<int>(num_full);
-  p.num_units = static_cast<int>(num_units);
+  p.tiles_m = static_cast<int>(q.tiles_m);
+  p.tiles_n = static_cast<int>(q.tiles_n);
+  p.num_tiles = static_cast<int>(q.num_tiles);
+  p.num_full = static_cast<int>(q.num_full);
+  p.num_units = static_cast<int>(q.num_units);
   p.num_kb = static_cast<int>((K + gws::BK - 1) / gws::BK);
+  p.num_stages = static_cast<int>(q.num_stages);
+  p.ksplit = static_cast<int>(q.ksplit);
+  p.split_stages = static_cast<int>(q.split_stages);
+  p.partial = h->partial;
+  p.split_count = h->split_count;
   p.group_m = h->group_m;
   p.staging_tiles_m = static_cast<int>((M + gws::STAGING - 1) / gws::STAGING);
   p.staging_tiles_n = static_cast<int>(stn);
@@ -277,7 +341,7 @@ int launch(gemm_ws* h, const uint16_t* A, const uint16_t* B, const uint16_t* C, 
     // Programmatic stream serialisation: this grid may be scheduled while the
     // previous kernel in the stream finishes; it waits for that kernel before
     // its first global-memory access (grid_dependency_wait in the kernel).
-    const int64_t clusters = num_units < P ? num_units : P;
+    const int64_t clusters = q.clusters;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[2];
     int nattr = 0;
@@ -337,6 +401,14 @@ int cta_group_from_env() {
     if (std::atoi(s) == 1) return 1;
   }
   return 2;
+}
+
+// GEMM_WS_SPLIT_K=0 keeps every tile's K range whole (default: split-K on).
+int split_k_from_env() {
+  if (const char* s = std::getenv("GEMM_WS_SPLIT_K")) {
+    if (std::atoi(s) == 0) return 0;
+  }
+  return 1;
 }
 
 // GEMM_WS_GROUP_M overrides the raster group (m-tiles per n step; default 8).
@@ -404,13 +476,25 @@ int gemm_ws_create(gemm_ws_t** out, int device) {
   h->multicast = multicast_from_env();
   h->pdl = pdl_from_env();
   h->group_m = group_m_from_env();
+  h->split_k = split_k_from_env();
   e = configure_kernels(h->num_sms, &h->max_pair_clusters, &h->max_quad_clusters);
   if (e == cudaSuccess && h->max_quad_clusters < 1) h->multicast = 1;
   if (e == cudaSuccess && h->max_pair_clusters < 1) h->cta_group = 1;
   if (e == cudaSuccess) e = cudaMalloc(&h->work, kWorkWords * sizeof(uint32_t));
   if (e == cudaSuccess) e = cudaMemset(h->work, 0, kWorkWords * sizeof(uint32_t));
+  // Split-K workspace: a launch that splits has at most one unit per
+  // cluster, so at most one partial part and one counter per SM.
+  if (e == cudaSuccess)
+    e = cudaMalloc(&h->partial, static_cast<size_t>(h->num_sms) * kPartBytes);
+  if (e == cudaSuccess)
+    e = cudaMalloc(&h->split_count, static_cast<size_t>(h->num_sms) * kCountersPerPart * 4);
+  if (e == cudaSuccess)
+    e = cudaMemset(h->split_count, 0, static_cast<size_t>(h->num_sms) * kCountersPerPart * 4);
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
   if (e != cudaSuccess) {
     if (h->work) cudaFree(h->work);
+    if (h->partial) cudaFree(h->partial);
+    if (h->split_count) cudaFree(h->split_count);
     std::free(h);
     return GEMM_WS_ERR_CUDA;
   }
@@ -423,6 +507,8 @@ int gemm_ws_destroy(gemm_ws_t* h) {
   DeviceGuard guard(h->device);
   cudaDeviceSynchronize();
   cudaFree(h->work);
+  cudaFree(h->partial);
+  cudaFree(h->split_count);
   std::free(h);
   return GEMM_WS_OK;
 }
@@ -472,7 +558,12 @@ int gemm_ws_query_status(gemm_ws_t* h, void* stream) {
   e = cudaMemcpy(&st, h->work + 1, sizeof st, cudaMemcpyDeviceToHost);
   if (e != cudaSuccess) return cuda_fail(h, e);
   if (st != 0) {
-    e = cudaMemset(h->work + 1, 0, sizeof(uint32_t));
+    // An aborted launch may leave split-K counters and the stream-out
+    // counter part-way: start the next launch from zero.
+    e = cudaMemset(h->work, 0, kWorkWords * sizeof(uint32_t));
+    if (e == cudaSuccess)
+      e = cudaMemset(h->split_count, 0, static_cast<size_t>(h->num_sms) * kCountersPerPart * 4);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
     if (e != cudaSuccess) return cuda_fail(h, e);
   }
   return static_cast<int>(st);
@@ -500,19 +591,17 @@ int gemm_ws_debug_configure(gemm_ws_t* h, int fault, unsigned long long* trace) 
   return GEMM_WS_OK;
 }
 
-int gemm_ws_debug_launch_shape(gemm_ws_t* h, int64_t M, int64_t N, int64_t L, int* cta_group,
-                               int* clusters, int* num_tiles) {
-  if (!h || !cta_group || !clusters || !num_tiles || M <= 0 || N <= 0 || L <= 0)
+int gemm_ws_debug_launch_shape(gemm_ws_t* h, int64_t M, int64_t N, int64_t K, int64_t L,
+                               int streamout, int* ctas_per_cluster, int* clusters,
+                               int* num_units, int* ksplit) {
+  if (!h || !ctas_per_cluster || !clusters || !num_units || !ksplit || M <= 0 || N <= 0 ||
+      K < 0 || L <= 0)
     return GEMM_WS_ERR_INVALID_ARG;
-  const int cs = h->cta_group * (h->cta_group == 2 ? h->multicast : 1);
-  const int64_t tiles =
-      L * ((M + gws::BM * cs - 1) / (gws::BM * cs)) * ((N + gws::BN - 1) / gws::BN);
-  const int64_t cap = cluster_capacity(h, cs);
-  const int64_t full = choose_num_full(tiles, cap);
-  const int64_t units = full + 2 * (tiles - full);
-  *cta_group = cs;
-  *num_tiles = static_cast<int>(units);
-  *clusters = static_cast<int>(units < cap ? units : cap);
+  const Plan q = make_plan(h, M, N, K, L, streamout != 0);
+  *ctas_per_cluster = q.cs;
+  *num_units = static_cast<int>(q.num_units);
+  *clusters = static_cast<int>(q.clusters);
+  *ksplit = static_cast<int>(q.ksplit);
   return GEMM_WS_OK;
 }
 #endif

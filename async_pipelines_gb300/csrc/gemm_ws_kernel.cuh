@@ -72,6 +72,8 @@ constexpr int NUM_EPI_WARPS = 8;         // two per TMEM lane quarter
 constexpr int EPI_HALF_WARPS = 4;        // one per lane quarter: a half covers 128 rows
 constexpr int STAGING = 128;             // stream-out tile edge
 constexpr int SUB_PER_STAGING = STAGING / EPI_N;
+constexpr int SUB_PER_PART = BN / EPI_N;   // subtiles (32 x 32 chunks per lane quarter) of a part
+static_assert(SUB_PER_PART == 8, "split-K chunk rotation assumes four subtiles per epilogue warp");
 constexpr int WARP_TMA = 0;
 constexpr int WARP_MMA = 1;
 constexpr int WARP_EPI0 = 2;
@@ -148,7 +150,12 @@ struct Params {
   int M, N, K, L;
   int tiles_m, tiles_n, num_tiles, num_kb;   // tiles of 128*CG x 256
   int num_full;                  // tiles [0, num_full) run whole; the rest as two halves
-  int num_units;                 // num_full + 2 * (num_tiles - num_full)
+  int num_units;                 // work units (see unit_coords)
+  int num_stages;                // ring stages covering K (KSUB k-blocks each)
+  int ksplit;                    // > 1: every tile's k range is split this many ways
+  int split_stages;              // stages per split
+  float* partial;                // split partials: [tile][split][CTA][chunk] x 1024 fp32
+  uint32_t* split_count;         // [tile][CTA][chunk] pieces written (returned to 0)
   int group_m;                   // raster: tiles walk group_m m-tiles per n step
   int staging_tiles_m;           // ceil(M / 128)
   int staging_tiles_n;           // ceil(N / 128)
@@ -190,18 +197,36 @@ struct Unit {
   int mb, l;
   int n0;      // first column
   int width;   // 256 or 128 columns
+  int tile;    // tile index (for split-K bookkeeping)
+  int split;   // which k split (0 without split-K)
+  int kb0, kb1;   // ring stages [kb0, kb1) of the k range this unit covers
 };
 
+// With split-K (ksplit > 1) unit u is piece u % ksplit of tile u / ksplit:
+// every piece covers split_stages ring stages of K (a work unit with its own
+// k-tile start and count, as in the SM90 cooperative kernel's operator()),
+// and for every 32 x 32 chunk the piece that writes its partial last sums
+// all of them and runs the epilogue (that kernel's fixup / compute_epilogue
+// step, done here without any CTA waiting for another).
 __device__ __forceinline__ Unit unit_coords(const Params& p, int u) {
   Unit w;
   int t = u, half = -1;
-  if (u >= p.num_full) {
+  w.split = 0;
+  w.kb0 = 0;
+  w.kb1 = p.num_stages;
+  if (p.ksplit > 1) {
+    t = u / p.ksplit;
+    w.split = u - t * p.ksplit;
+    w.kb0 = w.split * p.split_stages;
+    w.kb1 = min(p.num_stages, w.kb0 + p.split_stages);
+  } else if (u >= p.num_full) {
     const int h = u - p.num_full;
     t = p.num_full + (h >> 1);
     half = h & 1;
   }
   int nb;
   tile_coords(p, t, w.mb, nb, w.l);
+  w.tile = t;
   w.n0 = nb * BN + (half > 0 ? BN / 2 : 0);
   w.width = half < 0 ? BN : BN / 2;
   return w;
@@ -372,8 +397,7 @@ __device__ __forceinline__ void producer_role(const Params& p, uint32_t sbase, u
     const bool whole = w.width == BN;
     const CUtensorMap* tmb = whole ? &p.tmB : &p.tmB2;
     const uint32_t tx = whole ? C::STAGE_TX : C::STAGE_TX_HALF;
-    const int num_stages = (p.num_kb + C::KSUB - 1) / C::KSUB;   // k extent, in stages
-    for (int kb = 0; kb < num_stages; ++kb) {
+    for (int kb = w.kb0; kb < w.kb1; ++kb) {
       const uint32_t s = g % C::STAGES;
       const uint32_t ph = (g / C::STAGES) & 1;
       if (!token && !wait_spin<MC == 2>(empty(s), ph ^ 1, wd)) {
@@ -447,13 +471,13 @@ __device__ __forceinline__ void mma_role(const Params& p, uint32_t sbase, uint32
   bool issued = false;
   for (int t = cluster; t < p.num_units; t += clusters, ++i) {
     const uint32_t b = i & 1, aph = (i >> 1) & 1;
-    const uint32_t idesc = unit_coords(p, t).width == BN ? C::IDESC : C::IDESC_HALF;
+    const Unit w = unit_coords(p, t);
+    const uint32_t idesc = w.width == BN ? C::IDESC : C::IDESC_HALF;
     if (!wait_spin<true>(bar(BAR_ACC_EMPTY + b), aph ^ 1, wd)) goto done;
     tc_fence_after_sync();   // epilogue's TMEM reads of buffer b precede these MMAs
     {
       const uint32_t d_tmem = tmem_base + b * BN;
-      const int num_stages = (p.num_kb + C::KSUB - 1) / C::KSUB;
-      for (int kb = 0; kb < num_stages; ++kb) {
+      for (int kb = w.kb0; kb < w.kb1; ++kb) {
         const uint32_t s = g % C::STAGES;
         // The stage's bytes are ordered before the MMA by the barrier's
         // transaction count (TMA and tcgen05 both act in the async proxy).
@@ -467,7 +491,7 @@ __device__ __forceinline__ void mma_role(const Params& p, uint32_t sbase, uint32
               sdesc_kmajor_sw128(a_addr + blk * C::A_BLOCK_BYTES + kin * UMMA_K * 2);
           const uint64_t bd =
               sdesc_kmajor_sw128(b_addr + blk * C::B_BLOCK_BYTES + kin * UMMA_K * 2);
-          const uint32_t acc = (kb | kk) != 0 ? 1u : 0u;
+          const uint32_t acc = (kb != w.kb0 || kk != 0) ? 1u : 0u;
           if constexpr (CG == 1)
             umma_bf16(d_tmem, ad, bd, idesc, acc);
           else
@@ -478,7 +502,7 @@ __device__ __forceinline__ void mma_role(const Params& p, uint32_t sbase, uint32
         ++g;
       }
     }
-    if (p.num_kb > 0) {
+    if (w.kb1 > w.kb0) {
       commit(bar(BAR_ACC_FULL + b), pair_mask);   // accumulator b complete in the pair
     } else {
       // K == 0: no MMA ran; signal the accumulator barriers directly.
@@ -545,6 +569,7 @@ __device__ __forceinline__ void epilogue_role(const Params& p, uint32_t sbase, u
     const int m0 = row_tile * BM + 32 * q, n0 = w.n0;
     const int nsub = staging_in_part(p, row_tile, w) * SUB_PER_STAGING;   // 0, 4 or 8
     const uint32_t b = i & 1, aph = (i >> 1) & 1;
+    const bool has_acc = w.kb1 > w.kb0;   // an MMA ran (K > 0)
 
     // One C buffer per warp: the load for a subtile is issued as soon as the
     // previous subtile's C has been read out of it.
@@ -569,38 +594,16 @@ __device__ __forceinline__ void epilogue_role(const Params& p, uint32_t sbase, u
           mbar_arrive_cluster(mapa_shared(bar(BAR_ACC_EMPTY + b), rank - rank % CG));
       }
     };
-    if (p.has_c && nsub > 0) issue_c(hf);
-
-    if (!warp_wait(bar(BAR_ACC_FULL + b), aph, wd)) break;
-    tc_fence_after_sync();
-#ifdef GEMM_WS_DEBUG
-    // stamp 0: this CTA's part of unit t has its accumulator (MMA done)
-    if (p.trace && q == (WARP_EPI0 & 3) && hf == 0 && lane == 0)
-      p.trace[(static_cast<size_t>(t) * C::CS + rank) * 2] = global_timer_ns();
-#endif
-    const uint32_t tacc = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + b * BN;
-    if (nsub == 0) release_acc();   // this CTA's rows lie outside M x N
-
-    bool ok = true;
-    for (int j = hf; j < nsub; j += 2) {
-      uint32_t acc[32];
-      if (p.num_kb > 0) {
-        tmem_ld_32x32b_x32(tacc + j * EPI_N, acc);
-        tmem_wait_ld();
-      } else {
-#pragma unroll
-        for (int x = 0; x < 32; ++x) acc[x] = 0u;
-      }
-      if (j + 2 >= nsub) release_acc();
-
-      float v[32];
-#pragma unroll
-      for (int x = 0; x < 32; ++x) v[x] = p.alpha * __uint_as_float(acc[x]);
+    // alpha * acc (+ beta * C), rounded to bf16, through a shared-memory slot
+    // to the TMA store of D (and, with stream-out, to the consumer warp).
+    // Returns false if a bounded wait gave up.
+    // alpha * acc (+ beta * C) of subtile j, rounded to bf16, through a
+    // shared-memory slot to the TMA store of D (and, with stream-out, to the
+    // consumer warp). next_c: the subtile whose C load may now reuse this
+    // warp's C buffer (-1: none). Returns false if a bounded wait gave up.
+    auto finish_subtile = [&](int j, float (&v)[32], int next_c) -> bool {
       if (p.has_c) {
-        if (!warp_wait_spin(cbar, cu & 1, wd)) {
-          ok = false;
-          break;
-        }
+        if (!warp_wait_spin(cbar, cu & 1, wd)) return false;
         const uint8_t* cq = smem + (cbuf - sbase) + row_off;
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
@@ -611,9 +614,8 @@ __device__ __forceinline__ void epilogue_role(const Params& p, uint32_t sbase, u
           for (int x = 0; x < 8; ++x) v[8 * c + x] = fmaf(p.beta, cf[x], v[8 * c + x]);
         }
         ++cu;
-        if (j + 2 < nsub) issue_c(j + 2);
+        if (next_c >= 0) issue_c(next_c);
       }
-
       // Reuse a slot only when (a) this warp's TMA store from it has
       // finished reading it and (b) the stream-out consumer released it.
       const uint32_t slot = hf + 2 * (u % per_half);
@@ -624,10 +626,7 @@ __device__ __forceinline__ void epilogue_role(const Params& p, uint32_t sbase, u
           bulk_wait_read<0>();
       }
       if (p.streamout) {
-        if (!warp_wait_spin(bar(BAR_D_EMPTY + slot), ((u / per_half) & 1) ^ 1, wd)) {
-          ok = false;
-          break;
-        }
+        if (!warp_wait_spin(bar(BAR_D_EMPTY + slot), ((u / per_half) & 1) ^ 1, wd)) return false;
       }
       __syncwarp();
       uint8_t* dq = smem + C::OFF_D + slot * EPI_SLOT_BYTES + q * EPI_QUARTER_BYTES;
@@ -648,6 +647,137 @@ __device__ __forceinline__ void epilogue_role(const Params& p, uint32_t sbase, u
         if (p.streamout) mbar_arrive(bar(BAR_D_FULL + slot));
       }
       ++u;
+      return true;
+    };
+
+    const bool split = p.ksplit > 1;
+    if (p.has_c && nsub > 0 && !split) issue_c(hf);
+
+    if (!warp_wait(bar(BAR_ACC_FULL + b), aph, wd)) break;
+    tc_fence_after_sync();
+#ifdef GEMM_WS_DEBUG
+    // stamp 0: this CTA's part of unit t has its accumulator (MMA done)
+    if (p.trace && q == (WARP_EPI0 & 3) && hf == 0 && lane == 0)
+      p.trace[(static_cast<size_t>(t) * C::CS + rank) * 2] = global_timer_ns();
+#endif
+    const uint32_t tacc = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + b * BN;
+
+    bool ok = true;
+    if (!split) {
+      if (nsub == 0) release_acc();   // this CTA's rows lie outside M x N
+      for (int j = hf; j < nsub; j += 2) {
+        uint32_t acc[32];
+        if (has_acc) {
+          tmem_ld_32x32b_x32(tacc + j * EPI_N, acc);
+          tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int x = 0; x < 32; ++x) acc[x] = 0u;
+        }
+        if (j + 2 >= nsub) release_acc();
+        float v[32];
+#pragma unroll
+        for (int x = 0; x < 32; ++x) v[x] = p.alpha * __uint_as_float(acc[x]);
+        if (!finish_subtile(j, v, j + 2 < nsub ? j + 2 : -1)) {
+          ok = false;
+          break;
+        }
+      }
+    } else {
+      // Split-K. The warp's four 32 x 32 chunks (its TMEM lane quarter q,
+      // subtiles j = hf, hf+2, ...) each go to the workspace in the TMEM
+      // register layout: float4 c of lane r at [c][r], so a warp's store or
+      // load is 512 contiguous bytes. Each chunk has its own arrival
+      // counter; the piece whose write completes the count adds the S
+      // partials of that chunk (in piece order: the bits do not depend on
+      // which piece it is) and runs the epilogue for it. Pieces start at
+      // different chunks, so when they finish together the chunks' last
+      // writers, and the reductions, spread over the pieces. Nothing waits
+      // for another CTA.
+      const size_t part = static_cast<size_t>(w.tile) * p.ksplit * C::CS + rank;   // piece 0
+      auto chunk_of = [&](int piece, int j) -> float* {
+        return p.partial +
+               (((part + static_cast<size_t>(piece) * C::CS) * 4 + q) * SUB_PER_PART + j) *
+                   (32 * EPI_N);
+      };
+      uint32_t mine = 0;   // bit j: this piece completed chunk j's count
+      for (int i = 0; i < SUB_PER_PART / 2; ++i) {
+        const int j = hf + 2 * ((i + w.split) & (SUB_PER_PART / 2 - 1));
+        if (j >= nsub) continue;   // outside N (or this CTA's rows outside M)
+        uint32_t acc[32];
+        tmem_ld_32x32b_x32(tacc + j * EPI_N, acc);
+        tmem_wait_ld();
+        float4* dst = reinterpret_cast<float4*>(chunk_of(w.split, j));
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+          __stcg(dst + c * 32 + lane,
+                 make_float4(__uint_as_float(acc[4 * c]), __uint_as_float(acc[4 * c + 1]),
+                             __uint_as_float(acc[4 * c + 2]), __uint_as_float(acc[4 * c + 3])));
+        __threadfence();   // this lane's partial before the count (cumulative via the warp)
+        __syncwarp();
+        uint32_t last = 0;
+        if (lane == 0) {
+          uint32_t* cnt =
+              p.split_count + ((static_cast<size_t>(w.tile) * C::CS + rank) * 4 + q) * SUB_PER_PART + j;
+          last = atomicAdd(cnt, 1u) == static_cast<uint32_t>(p.ksplit - 1) ? 1u : 0u;
+          if (last) atomicExch(cnt, 0u);   // all pieces in: ready for the next launch
+        }
+        mine |= __shfl_sync(0xffffffffu, last, 0) << j;
+      }
+      release_acc();
+      if (mine) __threadfence();   // the other pieces' partials, counted in before ours
+      // Chunks to finish, in increasing j; the C load of the first goes out now.
+      int j = mine ? __ffs(mine) - 1 : -1;
+      if (p.has_c && j >= 0) issue_c(j);
+      while (j >= 0) {
+        const uint32_t rest = mine & ~((2u << j) - 1u);
+        const int next = rest ? __ffs(rest) - 1 : -1;
+        float v[32];
+#pragma unroll
+        for (int x = 0; x < 32; ++x) v[x] = 0.0f;
+        int sk = 0;
+        for (; sk + 1 < p.ksplit; sk += 2) {
+          const float4* s0 = reinterpret_cast<const float4*>(chunk_of(sk, j)) + lane;
+          const float4* s1 = reinterpret_cast<const float4*>(chunk_of(sk + 1, j)) + lane;
+          float4 f0[8], f1[8];
+#pragma unroll
+          for (int c = 0; c < 8; ++c) f0[c] = __ldcg(s0 + c * 32);   // L2: other SMs wrote it
+#pragma unroll
+          for (int c = 0; c < 8; ++c) f1[c] = __ldcg(s1 + c * 32);
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            v[4 * c] += f0[c].x;
+            v[4 * c + 1] += f0[c].y;
+            v[4 * c + 2] += f0[c].z;
+            v[4 * c + 3] += f0[c].w;
+          }
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            v[4 * c] += f1[c].x;
+            v[4 * c + 1] += f1[c].y;
+            v[4 * c + 2] += f1[c].z;
+            v[4 * c + 3] += f1[c].w;
+          }
+        }
+        if (sk < p.ksplit) {
+          const float4* s0 = reinterpret_cast<const float4*>(chunk_of(sk, j)) + lane;
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const float4 f = __ldcg(s0 + c * 32);
+            v[4 * c] += f.x;
+            v[4 * c + 1] += f.y;
+            v[4 * c + 2] += f.z;
+            v[4 * c + 3] += f.w;
+          }
+        }
+#pragma unroll
+        for (int x = 0; x < 32; ++x) v[x] *= p.alpha;
+        if (!finish_subtile(j, v, next)) {
+          ok = false;
+          break;
+        }
+        j = next;
+      }
     }
     if (!ok) break;
   }

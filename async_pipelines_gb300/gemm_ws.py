@@ -95,7 +95,8 @@ def load_debug_library():
         lib.gemm_ws_debug_configure.restype = ctypes.c_int
         ip = ctypes.POINTER(ctypes.c_int)
         lib.gemm_ws_debug_launch_shape.argtypes = [ctypes.c_void_p, ctypes.c_int64,
-                                                   ctypes.c_int64, ctypes.c_int64, ip, ip, ip]
+                                                   ctypes.c_int64, ctypes.c_int64,
+                                                   ctypes.c_int64, ctypes.c_int, ip, ip, ip, ip]
         lib.gemm_ws_debug_launch_shape.restype = ctypes.c_int
         _debug_lib = lib
     return _debug_lib

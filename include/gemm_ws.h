@@ -25,8 +25,13 @@
  *
  * Ownership: every data pointer is a borrowed DEVICE pointer on the handle's
  * device; the caller owns it and keeps it alive until the stream work ends.
- * The handle owns only its small device workspace (the stream-out sequence
- * counter, a status word, a completion count).
+ * The handle owns only its device workspace: the stream-out sequence
+ * counter, a status word, a completion count, and the split-K area (one
+ * 128 x 256 fp32 partial and 32 arrival counters per SM, ~128 KiB per SM).
+ * The kernel returns every counter to zero before it ends, so runs need no
+ * clearing between them; runs on one handle that overlap on the GPU (e.g. on
+ * two streams) race on that workspace: serialise them or use one handle per
+ * stream.
  *
  * Errors: every entry point returns a gemm_ws_status. A call that returns an
  * error other than GEMM_WS_ERR_CUDA launched nothing and wrote nothing. All
@@ -74,7 +79,13 @@ int gemm_ws_destroy(gemm_ws_t* h);
  *  - K % 8 == 0 and N % 8 == 0 (16-byte row pitches); pointers 16-byte aligned.
  *  - K == 0 gives D = beta * C (or 0); M*N*L == 0 launches nothing.
  *  - D must not overlap A or B; D may be exactly C (in place).
- * Rounding: fp32 alpha * acc + beta * c, then round-to-nearest-even to bf16. */
+ * Rounding: fp32 alpha * acc + beta * c, then round-to-nearest-even to bf16.
+ * Split-K: when the output has at most half as many tiles as the GPU has
+ * persistent clusters and K >= 2048, each tile's K range is cut into 2..32
+ * pieces of >= 1024 that run on separate clusters; acc is then the sum, in
+ * piece order, of the pieces' fp32 partials (deterministic: the same bits on
+ * every run). GEMM_WS_SPLIT_K=0 in the environment at gemm_ws_create turns
+ * it off for that handle. gemm_ws_run_streamout never splits. */
 int gemm_ws_run(gemm_ws_t* h, const uint16_t* A, const uint16_t* B,
                 const uint16_t* C, uint16_t* D, int64_t M, int64_t N, int64_t K,
                 int64_t L, float alpha, float beta, void* stream);

@@ -26,10 +26,9 @@ extern "C" {
 /* Sets the handle's debug state for its later runs.
  *  - fault: 0 none; 1 the stream-out consumer warp returns at once, so the
  *    epilogue's wait for a free slot can only end by the watchdog.
- *  - trace: device buffer of num_units * cta_group * 2 uint64 (see
- *    gemm_ws_debug_launch_shape; cta_group there is the number of CTAs per
- *    cluster) or NULL. For work unit u and CTA rank r in its cluster,
- *    trace[(u*cta_group + r)*2] = global time (ns) at which
+ *  - trace: device buffer of num_units * ctas_per_cluster * 2 uint64 (see
+ *    gemm_ws_debug_launch_shape) or NULL. For work unit u and CTA rank r
+ *    in its cluster, trace[(u*ctas_per_cluster + r)*2] = global time (ns) at which
  *    that CTA's epilogue saw the unit's accumulator complete, and [...+1] =
  *    time at which its consumer published the last stream-out tile of that
  *    part (written only by gemm_ws_run_streamout; untouched where the part
@@ -37,12 +36,18 @@ extern "C" {
  * Returns GEMM_WS_OK or GEMM_WS_ERR_INVALID_ARG. */
 int gemm_ws_debug_configure(gemm_ws_t* h, int fault, unsigned long long* trace);
 
-/* The launch the handle would make for an M x N x L problem: CTAs per
- * cluster (1, 2, or 4 with B multicast), number of clusters (persistent CTA groups; cluster c takes work
- * units c, c + clusters, ...) and number of work units (whole 256-column
- * tiles, then the last tiles as two 128-column halves). Host arithmetic only. */
-int gemm_ws_debug_launch_shape(gemm_ws_t* h, int64_t M, int64_t N, int64_t L,
-                               int* cta_group, int* clusters, int* num_units);
+/* The launch the handle would make for an M x N x K x L problem (streamout:
+ * nonzero for gemm_ws_run_streamout, 0 for gemm_ws_run): CTAs per cluster
+ * (1, 2, or 4 with B multicast), number of clusters (persistent CTA groups;
+ * cluster c takes work units c, c + clusters, ...), number of work units and
+ * the split-K factor. Without split-K (ksplit == 1) the units are the whole
+ * 256-column tiles, then the last tiles as two 128-column halves; with it,
+ * unit u is k-range piece u % ksplit of tile u / ksplit. Host arithmetic only.
+ * Returns GEMM_WS_OK or GEMM_WS_ERR_INVALID_ARG (null output pointer, M, N or
+ * L below 1, K below 0). */
+int gemm_ws_debug_launch_shape(gemm_ws_t* h, int64_t M, int64_t N, int64_t K, int64_t L,
+                               int streamout, int* ctas_per_cluster, int* clusters,
+                               int* num_units, int* ksplit);
 
 #ifdef __cplusplus
 }

@@ -32,13 +32,13 @@ def debug_handle(cta_group: int = 2, timeout_ms: int = 1000,
         return gemm_ws.GemmWS(0, lib=lib)
 
 
-def launch_shape(g: gemm_ws.GemmWS, M: int, N: int, L: int):
-    """(CTAs per cluster, clusters, work units) of the handle's launch."""
-    cg, cl, nt = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
-    rc = g.lib.gemm_ws_debug_launch_shape(g.handle, M, N, L, ctypes.byref(cg),
-                                          ctypes.byref(cl), ctypes.byref(nt))
+def launch_shape(g: gemm_ws.GemmWS, M: int, N: int, K: int, L: int, streamout: bool = True):
+    """(CTAs per cluster, clusters, work units, split-K factor) of the handle's launch."""
+    cg, cl, nu, ks = ctypes.c_int(), ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+    rc = g.lib.gemm_ws_debug_launch_shape(g.handle, M, N, K, L, int(streamout), ctypes.byref(cg),
+                                          ctypes.byref(cl), ctypes.byref(nu), ctypes.byref(ks))
     assert rc == gemm_ws.OK
-    return cg.value, cl.value, nt.value
+    return cg.value, cl.value, nu.value, ks.value
 
 
 def configure(g: gemm_ws.GemmWS, fault: int, trace_ptr=None):
