@@ -37,10 +37,10 @@ struct gemm_ws {
   int max_quad_clusters;          // co-resident 4-CTA clusters of the multicast kernel
   int group_m;                    // raster group: m-tiles walked per n step
   int max_pair_clusters;          // co-resident 2-CTA clusters of the pair kernel
-  int split_k;                    // allow split-K for few-tile, long-K problems
+  int stream_k;                   // 0 off, 1 where the cost model gains (default), 2 always
   uint32_t* work;                 // [0] stream-out counter, [1] status, [2] done count
-  float* partial;                 // split-K partials: num_sms parts of 128 x 256 fp32
-  uint32_t* split_count;          // split-K arrival counters, num_sms * 32 words (kept at zero)
+  float* partial;                 // stream-K partials: 3 * num_sms parts of 128 x 256 fp32
+  uint32_t* split_count;          // stream-K chunk counters, 2 * num_sms * 32 words (kept at zero)
   int last_cuda_error;
   unsigned long long timeout_ns;
   PFN_cuTensorMapEncodeTiled_v12000 encode;
@@ -135,10 +135,14 @@ int check_problem(gemm_ws* h, const uint16_t* A, const uint16_t* B, const uint16
 // units so that the persistent schedule's final wave is not half idle.
 // Cluster c runs units c, c + P, ...; a whole tile costs 1, a half ~0.6 (same
 // k-loop and A traffic, half the MMA work). Returns the number of whole
-// tiles; only splits of at most one wave of tiles are considered (with fewer
-// tiles than clusters, splitting spreads a small problem over more SMs).
-int64_t choose_num_full(int64_t tiles, int64_t P) {
-  if (P <= 1) return tiles;
+// tiles (and, in *cost, the slowest cluster's work in tile units); only
+// splits of at most one wave of tiles are considered (with fewer tiles than
+// clusters, splitting spreads a small problem over more SMs).
+int64_t choose_num_full(int64_t tiles, int64_t P, double* cost) {
+  if (P <= 1) {
+    *cost = static_cast<double>(tiles);
+    return tiles;
+  }
   // Cluster c gets ceil-or-floor shares of both the units and the whole
   // tiles, both non-increasing in c, so cluster 0 is always the slowest.
   double best = 0.0;
@@ -153,6 +157,7 @@ int64_t choose_num_full(int64_t tiles, int64_t P) {
       best_full = F;
     }
   }
+  *cost = best;
   return best_full;
 }
 
@@ -202,26 +207,47 @@ int64_t cluster_capacity(const gemm_ws* h, int cs) {
   return cs == 1 ? h->num_sms : (cs == 2 ? h->max_pair_clusters : h->max_quad_clusters);
 }
 
-// Split-K is used when the output has at most half as many tiles as the GPU
-// has persistent clusters and K is long: each tile's K range is cut into
-// `ksplit` pieces of at least kMinSplitK elements, run as separate units;
-// for every 32 x 32 chunk, the piece that writes its fp32 partial last sums
-// all of them. Every split unit runs in the first (only) wave, so the
-// workspace needs at most one 128 x 256 fp32 part (and one set of chunk
-// counters) per CTA of the launch.
-constexpr int64_t kMinSplitK = 1024;
-constexpr int64_t kMaxSplit = 32;
+// Stream-K. The tiles of a stream-K region pool their ring stages and
+// clusters take equal contiguous shares, cut at tile edges into pieces; a
+// tile computed by several pieces gets its fp32 partials summed, per 32 x 32
+// chunk, by the piece that writes that chunk last.
+//  - Default (GEMM_WS_STREAM_K=1): only problems with no more tiles than
+//    half the clusters, as split-K: every tile's K range is cut into S equal
+//    pieces of >= kMinShareK (S <= kMaxSplit), one per cluster, so pieces
+//    with the same index start at the same k on every tile and share their
+//    A and B panels through L2. Used where the host cost model (in
+//    tile-times of the slowest cluster; kPieceCostStages per piece edge for
+//    the partial write, the reduction and the pipeline restart) beats whole
+//    tiles with split halves.
+//  - GEMM_WS_STREAM_K=2 (tests, and callers who measured a gain): also
+//    uneven shares over all clusters, and, with more tiles than clusters, a
+//    stream-K region made of the last partial wave (plus one full wave if it
+//    is under half full) after whole-tile waves. Measured slower than whole
+//    tiles on every such shape tried on GB300: staggered k positions break
+//    the L2 sharing of A and B panels between concurrent tiles, and short
+//    pieces leave the MMA waiting for the epilogue.
+constexpr int64_t kMinShareK = 1024;
+constexpr int64_t kMaxSplit = 16;
+constexpr double kPieceCostStages = 4.0;
 constexpr size_t kPartBytes = size_t{gws::BM} * gws::BN * sizeof(float);
 // One counter per 32 x 32 chunk of a part: 4 lane quarters x 8 subtiles.
 constexpr size_t kCountersPerPart = 4 * gws::SUB_PER_PART;
+// Workspace bounds (per SM): partial parts and chunk-counter sets.
+constexpr size_t kPartsPerSm = gws::SK_MAX_PIECES_PER_CLUSTER;
+constexpr size_t kCounterSetsPerSm = 2;
+#ifdef GEMM_WS_DEBUG
+constexpr int kScheduleCols = 15;   // columns of a gemm_ws_debug_schedule row
+#endif
 
 struct Plan {
   int cs;              // CTAs per cluster
   int64_t tiles_m, tiles_n, num_tiles;
   int64_t num_full;    // whole-width units (the rest of the tiles run as halves)
-  int64_t num_units;
+  int64_t num_units;   // units (an upper bound of unit ids with stream-K)
   int64_t num_stages;  // ring stages covering K
-  int64_t ksplit, split_stages;
+  int64_t sk_first;    // first tile of the stream-K region (num_tiles: none)
+  int64_t sk_clusters; // clusters sharing the stream-K region
+  int64_t sk_work;     // ring stages in the stream-K region
   int64_t clusters;    // persistent clusters launched
 };
 
@@ -235,32 +261,53 @@ Plan make_plan(const gemm_ws* h, int64_t M, int64_t N, int64_t K, int64_t L, boo
   q.tiles_n = (N + gws::BN - 1) / gws::BN;
   q.num_tiles = L * q.tiles_m * q.tiles_n;
   const int64_t ksub = cg == 1 ? gws::Cfg<1, 1>::KSUB : gws::Cfg<2, 1>::KSUB;
-  q.num_stages = ((K + gws::BK - 1) / gws::BK + ksub - 1) / ksub;
+  const int64_t T = q.num_tiles;
+  const int64_t ns = ((K + gws::BK - 1) / gws::BK + ksub - 1) / ksub;
+  q.num_stages = ns;
   const int64_t P = cluster_capacity(h, q.cs);
-  q.ksplit = 1;
-  q.split_stages = q.num_stages;
-  // Stream-out keeps whole tiles: its consumer takes every tile where it is
-  // computed.
-  if (!streamout && h->split_k && h->partial && 2 * q.num_tiles <= P) {
-    int64_t S = P / q.num_tiles;
-    const int64_t by_k = K / kMinSplitK;
-    if (S > by_k) S = by_k;
-    if (S > kMaxSplit) S = kMaxSplit;
-    if (S > q.num_stages) S = q.num_stages;
-    if (S >= 2) {
-      q.split_stages = (q.num_stages + S - 1) / S;
-      q.ksplit = (q.num_stages + q.split_stages - 1) / q.split_stages;   // none empty
-      if (q.ksplit < 2) q.split_stages = q.num_stages, q.ksplit = 1;
-    }
-  }
-  if (q.ksplit > 1) {
-    q.num_full = q.num_tiles;
-    q.num_units = q.num_tiles * q.ksplit;
-  } else {
-    q.num_full = choose_num_full(q.num_tiles, P);
-    q.num_units = q.num_full + 2 * (q.num_tiles - q.num_full);
-  }
+  double dp_cost = 0.0;
+  q.num_full = choose_num_full(T, P, &dp_cost);
+  q.num_units = q.num_full + 2 * (T - q.num_full);
   q.clusters = q.num_units < P ? q.num_units : P;
+  q.sk_first = T;
+  q.sk_clusters = 0;
+  q.sk_work = 0;
+  // Stream-out keeps whole tiles: its consumer takes every tile where the
+  // epilogue computes it.
+  if (streamout || h->stream_k == 0 || !h->partial || P < 2) return q;
+  const int64_t min_share = h->stream_k == 2 ? 1 : kMinShareK / (gws::BK * ksub);
+  if (ns < 2 * min_share) return q;
+  int64_t F, Pe;
+  if (h->stream_k == 1) {
+    if (2 * T > P) return q;
+    int64_t S = P / T;
+    if (S > ns / min_share) S = ns / min_share;
+    if (S > kMaxSplit) S = kMaxSplit;
+    if (S < 2) return q;
+    F = 0;
+    Pe = T * S;
+  } else if (T <= P) {
+    F = 0;
+    Pe = T * ns / min_share;
+    if (Pe > P) Pe = P;
+  } else {
+    const int64_t R = T % P;
+    if (R == 0) return q;
+    F = T - R - (2 * R < P ? P : 0);
+    Pe = P;
+  }
+  const int64_t W = (T - F) * ns;
+  const int64_t share = (W + Pe - 1) / Pe;
+  if (Pe < 2 || share > 2 * ns + 1) return q;   // would touch more than three tiles
+  const double sk_cost = static_cast<double>(F / P) + static_cast<double>(share) / ns +
+                         2.0 * kPieceCostStages / static_cast<double>(ns);
+  if (h->stream_k != 2 && !(sk_cost < dp_cost - 1e-9)) return q;
+  q.sk_first = F;
+  q.sk_clusters = Pe;
+  q.sk_work = W;
+  q.num_full = T;
+  q.num_units = F + Pe * gws::SK_MAX_PIECES_PER_CLUSTER;
+  q.clusters = F > 0 ? P : Pe;
   return q;
 }
 
@@ -315,8 +362,9 @@ int launch(gemm_ws* h, const uint16_t* A, const uint16_t* B, const uint16_t* C, 
   p.num_units = static_cast<int>(q.num_units);
   p.num_kb = static_cast<int>((K + gws::BK - 1) / gws::BK);
   p.num_stages = static_cast<int>(q.num_stages);
-  p.ksplit = static_cast<int>(q.ksplit);
-  p.split_stages = static_cast<int>(q.split_stages);
+  p.sk_first = static_cast<int>(q.sk_first);
+  p.sk_clusters = static_cast<int>(q.sk_clusters);
+  p.sk_work = q.sk_work;
   p.partial = h->partial;
   p.split_count = h->split_count;
   p.group_m = h->group_m;
@@ -403,10 +451,13 @@ int cta_group_from_env() {
   return 2;
 }
 
-// GEMM_WS_SPLIT_K=0 keeps every tile's K range whole (default: split-K on).
-int split_k_from_env() {
-  if (const char* s = std::getenv("GEMM_WS_SPLIT_K")) {
-    if (std::atoi(s) == 0) return 0;
+// GEMM_WS_STREAM_K: 0 keeps every tile's K range whole; 2 uses stream-K
+// wherever the schedule allows it (tests); default 1: where the host cost
+// model expects a gain.
+int stream_k_from_env() {
+  if (const char* s = std::getenv("GEMM_WS_STREAM_K")) {
+    const int v = std::atoi(s);
+    if (v == 0 || v == 2) return v;
   }
   return 1;
 }
@@ -476,20 +527,19 @@ int gemm_ws_create(gemm_ws_t** out, int device) {
   h->multicast = multicast_from_env();
   h->pdl = pdl_from_env();
   h->group_m = group_m_from_env();
-  h->split_k = split_k_from_env();
+  h->stream_k = stream_k_from_env();
   e = configure_kernels(h->num_sms, &h->max_pair_clusters, &h->max_quad_clusters);
   if (e == cudaSuccess && h->max_quad_clusters < 1) h->multicast = 1;
   if (e == cudaSuccess && h->max_pair_clusters < 1) h->cta_group = 1;
   if (e == cudaSuccess) e = cudaMalloc(&h->work, kWorkWords * sizeof(uint32_t));
   if (e == cudaSuccess) e = cudaMemset(h->work, 0, kWorkWords * sizeof(uint32_t));
-  // Split-K workspace: a launch that splits has at most one unit per
-  // cluster, so at most one partial part and one counter per SM.
+  // Stream-K workspace: each cluster runs at most three pieces (one partial
+  // part per CTA each), and the region holds under two waves of tiles.
+  const size_t counter_bytes = h->num_sms * kCounterSetsPerSm * kCountersPerPart * 4;
   if (e == cudaSuccess)
-    e = cudaMalloc(&h->partial, static_cast<size_t>(h->num_sms) * kPartBytes);
-  if (e == cudaSuccess)
-    e = cudaMalloc(&h->split_count, static_cast<size_t>(h->num_sms) * kCountersPerPart * 4);
-  if (e == cudaSuccess)
-    e = cudaMemset(h->split_count, 0, static_cast<size_t>(h->num_sms) * kCountersPerPart * 4);
+    e = cudaMalloc(&h->partial, static_cast<size_t>(h->num_sms) * kPartsPerSm * kPartBytes);
+  if (e == cudaSuccess) e = cudaMalloc(&h->split_count, counter_bytes);
+  if (e == cudaSuccess) e = cudaMemset(h->split_count, 0, counter_bytes);
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
   if (e != cudaSuccess) {
     if (h->work) cudaFree(h->work);
@@ -562,7 +612,8 @@ int gemm_ws_query_status(gemm_ws_t* h, void* stream) {
     // counter part-way: start the next launch from zero.
     e = cudaMemset(h->work, 0, kWorkWords * sizeof(uint32_t));
     if (e == cudaSuccess)
-      e = cudaMemset(h->split_count, 0, static_cast<size_t>(h->num_sms) * kCountersPerPart * 4);
+      e = cudaMemset(h->split_count, 0,
+                     static_cast<size_t>(h->num_sms) * kCounterSetsPerSm * kCountersPerPart * 4);
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
     if (e != cudaSuccess) return cuda_fail(h, e);
   }
@@ -593,15 +644,91 @@ int gemm_ws_debug_configure(gemm_ws_t* h, int fault, unsigned long long* trace) 
 
 int gemm_ws_debug_launch_shape(gemm_ws_t* h, int64_t M, int64_t N, int64_t K, int64_t L,
                                int streamout, int* ctas_per_cluster, int* clusters,
-                               int* num_units, int* ksplit) {
-  if (!h || !ctas_per_cluster || !clusters || !num_units || !ksplit || M <= 0 || N <= 0 ||
+                               int* num_units, int* sk_tiles) {
+  if (!h || !ctas_per_cluster || !clusters || !num_units || !sk_tiles || M <= 0 || N <= 0 ||
       K < 0 || L <= 0)
     return GEMM_WS_ERR_INVALID_ARG;
   const Plan q = make_plan(h, M, N, K, L, streamout != 0);
   *ctas_per_cluster = q.cs;
   *num_units = static_cast<int>(q.num_units);
   *clusters = static_cast<int>(q.clusters);
-  *ksplit = static_cast<int>(q.ksplit);
+  *sk_tiles = static_cast<int>(q.num_tiles - q.sk_first);
+  return GEMM_WS_OK;
+}
+
+int gemm_ws_debug_schedule(int cta_group, int multicast, int num_sms, int max_clusters,
+                           int stream_k, int64_t M, int64_t N, int64_t K, int64_t L,
+                           int streamout, int* rows, int64_t max_rows, int64_t* num_rows,
+                           int* plan) {
+  if ((cta_group != 1 && cta_group != 2) || (multicast != 1 && multicast != 2) ||
+      num_sms < 1 || max_clusters < 1 || !num_rows || !plan || M <= 0 || N <= 0 || K < 0 ||
+      L <= 0 || stream_k < 0 || stream_k > 2)
+    return GEMM_WS_ERR_INVALID_ARG;
+  gemm_ws h;
+  std::memset(&h, 0, sizeof h);
+  h.num_sms = num_sms;
+  h.cta_group = cta_group;
+  h.multicast = cta_group == 2 ? multicast : 1;
+  h.max_pair_clusters = max_clusters;
+  h.max_quad_clusters = max_clusters;
+  if (h.cta_group == 1) h.num_sms = max_clusters;
+  h.group_m = 8;
+  h.stream_k = stream_k;
+  float dummy = 0.0f;
+  h.partial = &dummy;   // only tested for null by the plan
+  const Plan q = make_plan(&h, M, N, K, L, streamout != 0);
+  gws::Params p;
+  std::memset(&p, 0, sizeof p);
+  p.M = static_cast<int>(M);
+  p.N = static_cast<int>(N);
+  p.K = static_cast<int>(K);
+  p.L = static_cast<int>(L);
+  p.tiles_m = static_cast<int>(q.tiles_m);
+  p.tiles_n = static_cast<int>(q.tiles_n);
+  p.num_tiles = static_cast<int>(q.num_tiles);
+  p.num_full = static_cast<int>(q.num_full);
+  p.num_units = static_cast<int>(q.num_units);
+  p.num_stages = static_cast<int>(q.num_stages);
+  p.sk_first = static_cast<int>(q.sk_first);
+  p.sk_clusters = static_cast<int>(q.sk_clusters);
+  p.sk_work = q.sk_work;
+  p.group_m = h.group_m;
+  plan[0] = q.cs;
+  plan[1] = static_cast<int>(q.clusters);
+  plan[2] = static_cast<int>(q.num_units);
+  plan[3] = static_cast<int>(q.num_tiles);
+  plan[4] = static_cast<int>(q.num_stages);
+  plan[5] = static_cast<int>(q.sk_first);
+  plan[6] = static_cast<int>(q.sk_clusters);
+  plan[7] = static_cast<int>(q.tiles_m);
+  plan[8] = static_cast<int>(q.tiles_n);
+  int64_t n = 0;
+  const int clusters = static_cast<int>(q.clusters);
+  for (int c = 0; c < clusters; ++c) {
+    gws::Unit w;
+    for (int i = 0; gws::next_unit(p, c, clusters, i, w); ++i) {
+      if (rows && n < max_rows) {
+        int* r = rows + n * kScheduleCols;
+        r[0] = c;
+        r[1] = i;
+        r[2] = w.id;
+        r[3] = w.tile;
+        r[4] = w.mb;
+        r[5] = w.n0;
+        r[6] = w.width;
+        r[7] = w.l;
+        r[8] = w.kb0;
+        r[9] = w.kb1;
+        r[10] = w.piece;
+        r[11] = w.pieces;
+        r[12] = w.sk_tile;
+        r[13] = w.first_cluster;
+        r[14] = w.pieces > 1 ? gws::sk_slot(p, w, w.piece) : -1;
+      }
+      ++n;
+    }
+  }
+  *num_rows = n;
   return GEMM_WS_OK;
 }
 #endif

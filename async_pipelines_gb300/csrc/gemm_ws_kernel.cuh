@@ -152,10 +152,14 @@ struct Params {
   int num_full;                  // tiles [0, num_full) run whole; the rest as two halves
   int num_units;                 // work units (see unit_coords)
   int num_stages;                // ring stages covering K (KSUB k-blocks each)
-  int ksplit;                    // > 1: every tile's k range is split this many ways
-  int split_stages;              // stages per split
-  float* partial;                // split partials: [tile][split][CTA][chunk] x 1024 fp32
-  uint32_t* split_count;         // [tile][CTA][chunk] pieces written (returned to 0)
+  // Stream-K: tiles [sk_first, num_tiles) pool their ring stages (sk_work in
+  // all) and sk_clusters clusters take equal shares; sk_first == num_tiles:
+  // no stream-K region.
+  int sk_first;
+  int sk_clusters;
+  long long sk_work;
+  float* partial;                // piece partials: [slot][CTA][chunk] x 1024 fp32
+  uint32_t* split_count;         // [stream-K tile][CTA][chunk] pieces written (returned to 0)
   int group_m;                   // raster: tiles walk group_m m-tiles per n step
   int staging_tiles_m;           // ceil(M / 128)
   int staging_tiles_n;           // ceil(N / 128)
@@ -177,59 +181,116 @@ struct Params {
 // Tile t -> (m block, n block, batch). Within a batch, tiles go down a group
 // of `group_m` m-blocks, then step n, so the CTAs resident at one time share
 // their A rows and B columns through L2.
-__device__ __forceinline__ void tile_coords(const Params& p, int t, int& mb, int& nb, int& l) {
+__host__ __device__ __forceinline__ void tile_coords(const Params& p, int t, int& mb, int& nb, int& l) {
   const int per_batch = p.tiles_m * p.tiles_n;
   l = t / per_batch;
   const int r = t - l * per_batch;
   const int group_tiles = p.group_m * p.tiles_n;
   const int g = r / group_tiles;
   const int first_m = g * p.group_m;
-  const int gm = min(p.tiles_m - first_m, p.group_m);
+  const int gm = p.tiles_m - first_m < p.group_m ? p.tiles_m - first_m : p.group_m;
   const int rr = r - g * group_tiles;
   mb = first_m + rr % gm;
   nb = rr / gm;
 }
 
-// A unit of work: a whole tile (256 columns) or, for the last tiles in
-// raster order, one half of a tile (128 columns), so that the final wave of
-// the persistent schedule is not left half idle.
+// A unit of work: a tile (256 columns, or, for the last tiles in raster
+// order, one 128-column half, so that the final wave of the persistent
+// schedule is not left half idle), or a piece of a tile's K range.
 struct Unit {
   int mb, l;
   int n0;      // first column
   int width;   // 256 or 128 columns
-  int tile;    // tile index (for split-K bookkeeping)
-  int split;   // which k split (0 without split-K)
-  int kb0, kb1;   // ring stages [kb0, kb1) of the k range this unit covers
+  int tile;    // tile index
+  int kb0, kb1;        // ring stages [kb0, kb1) of the tile's K range
+  int piece, pieces;   // piece `piece` of the `pieces` that share the K range (1: whole)
+  int sk_tile;         // index in the stream-K region (chunk counters)
+  int first_cluster;   // cluster that runs piece 0
+  int id;              // unit number (trace index)
 };
 
-// With split-K (ksplit > 1) unit u is piece u % ksplit of tile u / ksplit:
-// every piece covers split_stages ring stages of K (a work unit with its own
-// k-tile start and count, as in the SM90 cooperative kernel's operator()),
-// and for every 32 x 32 chunk the piece that writes its partial last sums
-// all of them and runs the epilogue (that kernel's fixup / compute_epilogue
-// step, done here without any CTA waiting for another).
-__device__ __forceinline__ Unit unit_coords(const Params& p, int u) {
+// Most pieces one cluster's share of the stream-K region can touch.
+constexpr int SK_MAX_PIECES_PER_CLUSTER = 3;
+
+__host__ __device__ __forceinline__ Unit whole_tile(const Params& p, int t) {
   Unit w;
-  int t = u, half = -1;
-  w.split = 0;
-  w.kb0 = 0;
-  w.kb1 = p.num_stages;
-  if (p.ksplit > 1) {
-    t = u / p.ksplit;
-    w.split = u - t * p.ksplit;
-    w.kb0 = w.split * p.split_stages;
-    w.kb1 = min(p.num_stages, w.kb0 + p.split_stages);
-  } else if (u >= p.num_full) {
-    const int h = u - p.num_full;
-    t = p.num_full + (h >> 1);
-    half = h & 1;
-  }
   int nb;
   tile_coords(p, t, w.mb, nb, w.l);
+  w.n0 = nb * BN;
+  w.width = BN;
   w.tile = t;
-  w.n0 = nb * BN + (half > 0 ? BN / 2 : 0);
-  w.width = half < 0 ? BN : BN / 2;
+  w.kb0 = 0;
+  w.kb1 = p.num_stages;
+  w.piece = 0;
+  w.pieces = 1;
+  w.sk_tile = -1;
+  w.first_cluster = 0;
+  w.id = t;
   return w;
+}
+
+// Without stream-K: unit u < num_full is tile u; the units after it are the
+// halves of the remaining tiles.
+__host__ __device__ __forceinline__ Unit unit_coords(const Params& p, int u) {
+  if (u < p.num_full) return whole_tile(p, u);
+  const int h = u - p.num_full;
+  Unit w = whole_tile(p, p.num_full + (h >> 1));
+  w.n0 += (h & 1) ? BN / 2 : 0;
+  w.width = BN / 2;
+  w.id = u;
+  return w;
+}
+
+// Stream-K region: tile r of it owns ring stages [r*ns, (r+1)*ns) of
+// sk_work = (#tiles) * ns; cluster c (< sk_clusters) owns stages
+// [c*sk_work/sk_clusters, (c+1)*sk_work/sk_clusters), cut at tile edges into
+// pieces (a work unit with its own k-tile start and count, as in the SM90
+// cooperative kernel's operator()). Every piece's place follows from this
+// arithmetic alone, so no role needs to exchange schedule information.
+__host__ __device__ __forceinline__ long long sk_begin(const Params& p, int c) {
+  return static_cast<long long>(c) * p.sk_work / p.sk_clusters;
+}
+// The cluster whose share holds stage s.
+__host__ __device__ __forceinline__ int sk_owner(const Params& p, long long s) {
+  return static_cast<int>(((s + 1) * p.sk_clusters - 1) / p.sk_work);
+}
+// Workspace slot of piece k of stream-K tile r: its cluster's j-th piece.
+__host__ __device__ __forceinline__ int sk_slot(const Params& p, const Unit& w, int k) {
+  const int c = w.first_cluster + k;
+  const int j = w.sk_tile - static_cast<int>(sk_begin(p, c) / p.num_stages);
+  return c * SK_MAX_PIECES_PER_CLUSTER + j;
+}
+
+// The i-th unit of cluster c (of `clusters`), in the order every role of the
+// cluster walks them; false once the cluster has no more.
+__host__ __device__ __forceinline__ bool next_unit(const Params& p, int c, int clusters, int i, Unit& w) {
+  if (p.sk_first >= p.num_tiles) {   // whole tiles, then halves: static stride
+    const int u = c + i * clusters;
+    if (u >= p.num_units) return false;
+    w = unit_coords(p, u);
+    return true;
+  }
+  const int dp = p.sk_first / clusters;   // whole tiles of each cluster (a multiple)
+  if (i < dp) {
+    w = whole_tile(p, c + i * clusters);
+    return true;
+  }
+  if (c >= p.sk_clusters) return false;
+  const int j = i - dp;
+  const long long ns = p.num_stages;
+  const long long s0 = sk_begin(p, c), s1 = sk_begin(p, c + 1);
+  const int r = static_cast<int>(s0 / ns) + j;
+  const long long ts = static_cast<long long>(r) * ns;
+  if (ts >= s1) return false;
+  w = whole_tile(p, p.sk_first + r);
+  w.kb0 = static_cast<int>((s0 > ts ? s0 : ts) - ts);
+  w.kb1 = static_cast<int>((s1 < ts + ns ? s1 : ts + ns) - ts);
+  w.first_cluster = sk_owner(p, ts);
+  w.pieces = sk_owner(p, ts + ns - 1) - w.first_cluster + 1;
+  w.piece = c - w.first_cluster;
+  w.sk_tile = r;
+  w.id = p.sk_first + c * SK_MAX_PIECES_PER_CLUSTER + j;
+  return true;
 }
 
 // Stream-out tiles (128 x 128) of this CTA's 128-row part of a unit that
@@ -384,8 +445,8 @@ __device__ __forceinline__ void producer_role(const Params& p, uint32_t sbase, u
   // The producer starts in the opposite phase: the first STAGES waits on a
   // freshly initialised empty barrier (parity 1) succeed at once.
   bool token = mbar_test_wait(empty(0), 1);
-  for (int t = cluster; ok && t < p.num_units; t += clusters) {
-    const Unit w = unit_coords(p, t);
+  Unit w;
+  for (int it = 0; ok && next_unit(p, cluster, clusters, it, w); ++it) {
     const int l = w.l;
     const int a_row = (w.mb * C::CS + static_cast<int>(rank)) * BM;   // this CTA's rows
     // B rows of this CTA's half of the pair's N; with multicast (MC == 2) each
@@ -469,9 +530,9 @@ __device__ __forceinline__ void mma_role(const Params& p, uint32_t sbase, uint32
   uint32_t g = 0;
   int i = 0;
   bool issued = false;
-  for (int t = cluster; t < p.num_units; t += clusters, ++i) {
+  Unit w;
+  for (; next_unit(p, cluster, clusters, i, w); ++i) {
     const uint32_t b = i & 1, aph = (i >> 1) & 1;
-    const Unit w = unit_coords(p, t);
     const uint32_t idesc = w.width == BN ? C::IDESC : C::IDESC_HALF;
     if (!wait_spin<true>(bar(BAR_ACC_EMPTY + b), aph ^ 1, wd)) goto done;
     tc_fence_after_sync();   // epilogue's TMEM reads of buffer b precede these MMAs
@@ -562,8 +623,8 @@ __device__ __forceinline__ void epilogue_role(const Params& p, uint32_t sbase, u
   uint32_t cu = 0;       // C subtiles consumed by this warp
   uint32_t c_issued = 0; // C subtile loads issued by this warp
   int i = 0;
-  for (int t = cluster; t < p.num_units; t += clusters, ++i) {
-    const Unit w = unit_coords(p, t);
+  Unit w;
+  for (; next_unit(p, cluster, clusters, i, w); ++i) {
     const int l = w.l;
     const int row_tile = w.mb * C::CS + static_cast<int>(rank);   // this CTA's 128-row slab
     const int m0 = row_tile * BM + 32 * q, n0 = w.n0;
@@ -650,15 +711,15 @@ __device__ __forceinline__ void epilogue_role(const Params& p, uint32_t sbase, u
       return true;
     };
 
-    const bool split = p.ksplit > 1;
+    const bool split = w.pieces > 1;
     if (p.has_c && nsub > 0 && !split) issue_c(hf);
 
     if (!warp_wait(bar(BAR_ACC_FULL + b), aph, wd)) break;
     tc_fence_after_sync();
 #ifdef GEMM_WS_DEBUG
-    // stamp 0: this CTA's part of unit t has its accumulator (MMA done)
+    // stamp 0: this CTA's part of the unit has its accumulator (MMA done)
     if (p.trace && q == (WARP_EPI0 & 3) && hf == 0 && lane == 0)
-      p.trace[(static_cast<size_t>(t) * C::CS + rank) * 2] = global_timer_ns();
+      p.trace[(static_cast<size_t>(w.id) * C::CS + rank) * 2] = global_timer_ns();
 #endif
     const uint32_t tacc = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + b * BN;
 
@@ -684,48 +745,47 @@ __device__ __forceinline__ void epilogue_role(const Params& p, uint32_t sbase, u
         }
       }
     } else {
-      // Split-K. The warp's four 32 x 32 chunks (its TMEM lane quarter q,
+      // A piece of the tile's K range. The warp's four 32 x 32 chunks (its TMEM lane quarter q,
       // subtiles j = hf, hf+2, ...) each go to the workspace in the TMEM
       // register layout: float4 c of lane r at [c][r], so a warp's store or
       // load is 512 contiguous bytes. Each chunk has its own arrival
       // counter; the piece whose write completes the count adds the S
       // partials of that chunk (in piece order: the bits do not depend on
-      // which piece it is) and runs the epilogue for it. Pieces start at
+      // which piece it is) and runs the epilogue for it (the fixup /
+      // compute_epilogue step of the SM90 cooperative kernel). Pieces start at
       // different chunks, so when they finish together the chunks' last
       // writers, and the reductions, spread over the pieces. Nothing waits
       // for another CTA.
-      const size_t part = static_cast<size_t>(w.tile) * p.ksplit * C::CS + rank;   // piece 0
       auto chunk_of = [&](int piece, int j) -> float* {
-        return p.partial +
-               (((part + static_cast<size_t>(piece) * C::CS) * 4 + q) * SUB_PER_PART + j) *
-                   (32 * EPI_N);
+        const size_t part = static_cast<size_t>(sk_slot(p, w, piece)) * C::CS + rank;
+        return p.partial + ((part * 4 + q) * SUB_PER_PART + j) * (32 * EPI_N);
       };
       uint32_t mine = 0;   // bit j: this piece completed chunk j's count
       for (int i = 0; i < SUB_PER_PART / 2; ++i) {
-        const int j = hf + 2 * ((i + w.split) & (SUB_PER_PART / 2 - 1));
+        const int j = hf + 2 * ((i + w.piece) & (SUB_PER_PART / 2 - 1));
         if (j >= nsub) continue;   // outside N (or this CTA's rows outside M)
         uint32_t acc[32];
         tmem_ld_32x32b_x32(tacc + j * EPI_N, acc);
         tmem_wait_ld();
-        float4* dst = reinterpret_cast<float4*>(chunk_of(w.split, j));
+        float4* dst = reinterpret_cast<float4*>(chunk_of(w.piece, j));
 #pragma unroll
         for (int c = 0; c < 8; ++c)
           __stcg(dst + c * 32 + lane,
                  make_float4(__uint_as_float(acc[4 * c]), __uint_as_float(acc[4 * c + 1]),
                              __uint_as_float(acc[4 * c + 2]), __uint_as_float(acc[4 * c + 3])));
-        __threadfence();   // this lane's partial before the count (cumulative via the warp)
+        fence_acq_rel_gpu();   // this lane's partial before the count (the warp syncs below)
         __syncwarp();
         uint32_t last = 0;
         if (lane == 0) {
-          uint32_t* cnt =
-              p.split_count + ((static_cast<size_t>(w.tile) * C::CS + rank) * 4 + q) * SUB_PER_PART + j;
-          last = atomicAdd(cnt, 1u) == static_cast<uint32_t>(p.ksplit - 1) ? 1u : 0u;
+          uint32_t* cnt = p.split_count +
+                          ((static_cast<size_t>(w.sk_tile) * C::CS + rank) * 4 + q) * SUB_PER_PART + j;
+          last = atomicAdd(cnt, 1u) == static_cast<uint32_t>(w.pieces - 1) ? 1u : 0u;
           if (last) atomicExch(cnt, 0u);   // all pieces in: ready for the next launch
         }
         mine |= __shfl_sync(0xffffffffu, last, 0) << j;
       }
       release_acc();
-      if (mine) __threadfence();   // the other pieces' partials, counted in before ours
+      if (mine) fence_acq_rel_gpu();   // the other pieces' partials, counted in before ours
       // Chunks to finish, in increasing j; the C load of the first goes out now.
       int j = mine ? __ffs(mine) - 1 : -1;
       if (p.has_c && j >= 0) issue_c(j);
@@ -736,7 +796,7 @@ __device__ __forceinline__ void epilogue_role(const Params& p, uint32_t sbase, u
 #pragma unroll
         for (int x = 0; x < 32; ++x) v[x] = 0.0f;
         int sk = 0;
-        for (; sk + 1 < p.ksplit; sk += 2) {
+        for (; sk + 1 < w.pieces; sk += 2) {
           const float4* s0 = reinterpret_cast<const float4*>(chunk_of(sk, j)) + lane;
           const float4* s1 = reinterpret_cast<const float4*>(chunk_of(sk + 1, j)) + lane;
           float4 f0[8], f1[8];
@@ -759,7 +819,7 @@ __device__ __forceinline__ void epilogue_role(const Params& p, uint32_t sbase, u
             v[4 * c + 3] += f1[c].w;
           }
         }
-        if (sk < p.ksplit) {
+        if (sk < w.pieces) {
           const float4* s0 = reinterpret_cast<const float4*>(chunk_of(sk, j)) + lane;
 #pragma unroll
           for (int c = 0; c < 8; ++c) {
@@ -800,8 +860,8 @@ __device__ __forceinline__ void consumer_role(const Params& p, uint32_t sbase, u
   // Each stream-out tile has exactly one publishing consumer, which clears
   // the tile's flag words before anything else; so no host-side clearing is
   // needed and nothing in this launch can observe a stale ready word.
-  for (int t = cluster; t < p.num_units; t += clusters) {
-    const Unit w = unit_coords(p, t);
+  Unit w;
+  for (int it = 0; next_unit(p, cluster, clusters, it, w); ++it) {
     const int row_tile = w.mb * C::CS + static_cast<int>(rank);
     const int nst = staging_in_part(p, row_tile, w);
     for (int st = 0; st < nst; ++st) {
@@ -817,8 +877,7 @@ __device__ __forceinline__ void consumer_role(const Params& p, uint32_t sbase, u
 #ifdef GEMM_WS_DEBUG
   if (p.debug_fault == 1) goto done;   // injected fault: no tile is ever taken
 #endif
-  for (int t = cluster; t < p.num_units; t += clusters) {
-    const Unit w = unit_coords(p, t);
+  for (int it = 0; next_unit(p, cluster, clusters, it, w); ++it) {
     const int row_tile = w.mb * C::CS + static_cast<int>(rank);
     const int nst = staging_in_part(p, row_tile, w);
     for (int st = 0; st < nst; ++st) {
@@ -844,9 +903,9 @@ __device__ __forceinline__ void consumer_role(const Params& p, uint32_t sbase, u
       st_release_gpu(p.flags + 2 * tile_id + 1, 1u);
     }
 #ifdef GEMM_WS_DEBUG
-    // stamp 1: every stream-out tile of this CTA's part of tile t is published
+    // stamp 1: every stream-out tile of this CTA's part of the unit is published
     if (p.trace && nst > 0)
-      p.trace[(static_cast<size_t>(t) * C::CS + rank) * 2 + 1] = global_timer_ns();
+      p.trace[(static_cast<size_t>(w.id) * C::CS + rank) * 2 + 1] = global_timer_ns();
 #endif
   }
 done:

@@ -81,7 +81,8 @@ def load_library(path: Optional[str] = None):
     return lib
 
 
-DEBUG_EXPORTS = ("gemm_ws_debug_configure", "gemm_ws_debug_launch_shape")
+DEBUG_EXPORTS = ("gemm_ws_debug_configure", "gemm_ws_debug_launch_shape",
+                 "gemm_ws_debug_schedule")
 
 _debug_lib = None
 
@@ -98,6 +99,12 @@ def load_debug_library():
                                                    ctypes.c_int64, ctypes.c_int64,
                                                    ctypes.c_int64, ctypes.c_int, ip, ip, ip, ip]
         lib.gemm_ws_debug_launch_shape.restype = ctypes.c_int
+        i64 = ctypes.c_int64
+        lib.gemm_ws_debug_schedule.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                               ctypes.c_int, ctypes.c_int, i64, i64, i64, i64,
+                                               ctypes.c_int, ctypes.c_void_p, i64,
+                                               ctypes.POINTER(i64), ip]
+        lib.gemm_ws_debug_schedule.restype = ctypes.c_int
         _debug_lib = lib
     return _debug_lib
 

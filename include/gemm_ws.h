@@ -26,8 +26,8 @@
  * Ownership: every data pointer is a borrowed DEVICE pointer on the handle's
  * device; the caller owns it and keeps it alive until the stream work ends.
  * The handle owns only its device workspace: the stream-out sequence
- * counter, a status word, a completion count, and the split-K area (one
- * 128 x 256 fp32 partial and 32 arrival counters per SM, ~128 KiB per SM).
+ * counter, a status word, a completion count, and the split-K area (three
+ * 128 x 256 fp32 partials and 64 chunk counters per SM, ~384 KiB per SM).
  * The kernel returns every counter to zero before it ends, so runs need no
  * clearing between them; runs on one handle that overlap on the GPU (e.g. on
  * two streams) race on that workspace: serialise them or use one handle per
@@ -80,12 +80,15 @@ int gemm_ws_destroy(gemm_ws_t* h);
  *  - K == 0 gives D = beta * C (or 0); M*N*L == 0 launches nothing.
  *  - D must not overlap A or B; D may be exactly C (in place).
  * Rounding: fp32 alpha * acc + beta * c, then round-to-nearest-even to bf16.
- * Split-K: when the output has at most half as many tiles as the GPU has
- * persistent clusters and K >= 2048, each tile's K range is cut into 2..32
- * pieces of >= 1024 that run on separate clusters; acc is then the sum, in
- * piece order, of the pieces' fp32 partials (deterministic: the same bits on
- * every run). GEMM_WS_SPLIT_K=0 in the environment at gemm_ws_create turns
- * it off for that handle. gemm_ws_run_streamout never splits. */
+ * Split-K (stream-K pieces): when the output has at most half as many
+ * tiles as the GPU has persistent clusters and K >= 2048, each tile's K
+ * range is cut into 2..16 equal pieces of >= 1024 that run on separate
+ * clusters; acc is then the sum, in piece order, of the pieces' fp32
+ * partials (deterministic: the same bits on every run). GEMM_WS_STREAM_K in
+ * the environment at gemm_ws_create sets this per handle: 0 off, 1 (default)
+ * as described, 2 stream-K wherever the schedule allows it (uneven shares
+ * over all clusters, and a stream-K region after whole-tile waves).
+ * gemm_ws_run_streamout never splits. */
 int gemm_ws_run(gemm_ws_t* h, const uint16_t* A, const uint16_t* B,
                 const uint16_t* C, uint16_t* D, int64_t M, int64_t N, int64_t K,
                 int64_t L, float alpha, float beta, void* stream);

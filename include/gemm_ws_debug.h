@@ -38,16 +38,33 @@ int gemm_ws_debug_configure(gemm_ws_t* h, int fault, unsigned long long* trace);
 
 /* The launch the handle would make for an M x N x K x L problem (streamout:
  * nonzero for gemm_ws_run_streamout, 0 for gemm_ws_run): CTAs per cluster
- * (1, 2, or 4 with B multicast), number of clusters (persistent CTA groups;
- * cluster c takes work units c, c + clusters, ...), number of work units and
- * the split-K factor. Without split-K (ksplit == 1) the units are the whole
- * 256-column tiles, then the last tiles as two 128-column halves; with it,
- * unit u is k-range piece u % ksplit of tile u / ksplit. Host arithmetic only.
+ * (1, 2, or 4 with B multicast), number of clusters (persistent CTA groups),
+ * an upper bound of the work-unit ids (size the trace buffer with it) and
+ * the number of tiles in the stream-K region (0: every tile runs whole or
+ * as two halves). Host arithmetic only.
  * Returns GEMM_WS_OK or GEMM_WS_ERR_INVALID_ARG (null output pointer, M, N or
  * L below 1, K below 0). */
 int gemm_ws_debug_launch_shape(gemm_ws_t* h, int64_t M, int64_t N, int64_t K, int64_t L,
                                int streamout, int* ctas_per_cluster, int* clusters,
-                               int* num_units, int* ksplit);
+                               int* num_units, int* sk_tiles);
+
+/* The whole persistent schedule of a launch, on the host, without a handle
+ * or a GPU: the plan the library makes for a device with `num_sms` SMs on
+ * which `max_clusters` clusters of the chosen shape fit (cta_group 1 or 2,
+ * multicast 1 or 2, stream_k 0 off / 1 cost model / 2 always), and the units
+ * every cluster walks, produced by the kernel's own unit iterator.
+ *  - plan[9] = {CTAs per cluster, clusters, unit-id bound, tiles, ring
+ *    stages per tile, first stream-K tile, stream-K clusters, tiles_m,
+ *    tiles_n}.
+ *  - rows: NULL, or max_rows x 15 ints, one row per unit in cluster-then-
+ *    walk order: {cluster, i, id, tile, m block, first column, width,
+ *    batch, first stage, end stage, piece, pieces, stream-K tile, cluster of
+ *    piece 0, workspace slot (-1 for a whole tile)}; *num_rows = units.
+ * Returns GEMM_WS_OK or GEMM_WS_ERR_INVALID_ARG. */
+int gemm_ws_debug_schedule(int cta_group, int multicast, int num_sms, int max_clusters,
+                           int stream_k, int64_t M, int64_t N, int64_t K, int64_t L,
+                           int streamout, int* rows, int64_t max_rows, int64_t* num_rows,
+                           int* plan);
 
 #ifdef __cplusplus
 }

@@ -33,7 +33,7 @@ def debug_handle(cta_group: int = 2, timeout_ms: int = 1000,
 
 
 def launch_shape(g: gemm_ws.GemmWS, M: int, N: int, K: int, L: int, streamout: bool = True):
-    """(CTAs per cluster, clusters, work units, split-K factor) of the handle's launch."""
+    """(CTAs per cluster, clusters, unit-id bound, stream-K tiles) of the handle's launch."""
     cg, cl, nu, ks = ctypes.c_int(), ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
     rc = g.lib.gemm_ws_debug_launch_shape(g.handle, M, N, K, L, int(streamout), ctypes.byref(cg),
                                           ctypes.byref(cl), ctypes.byref(nu), ctypes.byref(ks))

@@ -27,8 +27,8 @@ pytestmark = pytest.mark.gpu
 def test_streamout_overlaps_mma(cta_group, multicast):
     w = workloads.WORKLOADS[workloads.STREAMOUT]
     g = debug_handle(cta_group=cta_group, multicast=multicast)
-    cg, clusters, tiles, ksplit = launch_shape(g, w.M, w.N, w.K, w.L)   # cg: CTAs per cluster
-    assert ksplit == 1
+    cg, clusters, tiles, sk_tiles = launch_shape(g, w.M, w.N, w.K, w.L)   # cg: CTAs per cluster
+    assert sk_tiles == 0
     assert cg == cta_group * (2 if multicast else 1)
     trace = torch.zeros(tiles * cg * 2, dtype=torch.int64, device="cuda")
     configure(g, fault=0, trace_ptr=trace.data_ptr())

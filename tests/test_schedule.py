@@ -1,0 +1,172 @@
+"""The persistent schedule, checked on the CPU (no GPU needed).
+
+The debug library runs the kernel's own unit iterator on the host
+(gemm_ws_debug_schedule) for a given device shape. These tests check, for
+many problem shapes, device shapes and stream-K settings, that
+
+- every ring stage of every output tile (both 128-column halves) is computed
+  by exactly one unit: nothing is skipped, nothing is done twice;
+- the pieces of a stream-K tile are numbered 0..n-1 by consecutive clusters,
+  in K order, and all agree on n and on the first cluster;
+- every workspace slot and chunk-counter index stays inside the buffers the
+  handle allocates (3 partial parts and 2 counter sets per SM), slots are
+  never shared, and unit ids are unique and below the reported bound;
+- no cluster walks more than three stream-K pieces and the stream-K shares
+  differ by at most one stage;
+- stream-out and GEMM_WS_STREAM_K=0 plans never use stream-K.
+"""
+from __future__ import annotations
+
+import ctypes
+
+import numpy as np
+import pytest
+
+from async_pipelines_gb300 import build as _build
+from async_pipelines_gb300 import gemm_ws
+
+BM, BN, BK = 128, 256, 64
+
+# (cta_group, multicast, SMs, clusters that fit): CTA pairs and single CTAs
+# on 152 and 148 SMs, and 4-CTA multicast clusters.
+DEVICES = [(2, 1, 152, 76), (1, 1, 152, 152), (2, 2, 152, 38), (2, 1, 148, 74)]
+DEVICE_IDS = ["pair152", "single152", "quad152", "pair148"]
+
+SHAPES = [
+    (256, 256, 8192, 1), (8192, 8192, 8192, 1), (4096, 4096, 4096, 1),
+    (5000, 3000, 4000, 4), (2048, 2048, 16384, 1), (1024, 1024, 32768, 1),
+    (128, 8, 2048, 1), (1000, 776, 20000, 1), (200, 296, 4096, 3), (8192, 8192, 64, 1),
+    (256, 256, 256, 1), (640, 1024, 384, 2), (4000, 4104, 96, 2), (1, 8, 8, 1),
+    (300, 520, 200, 2), (256, 256, 0, 1), (2048, 2048, 2048, 1), (4096, 2560, 1024, 1),
+    (320, 264, 8192, 2), (6144, 6144, 2048, 1),
+]
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if _build.stale(_build.DEBUG_LIB):
+        _build.build()
+    return gemm_ws.load_debug_library()
+
+
+def schedule(lib, dev, stream_k, M, N, K, L, streamout=False):
+    cg, mc, sms, maxc = dev
+    plan = (ctypes.c_int * 9)()
+    n = ctypes.c_int64()
+    rc = lib.gemm_ws_debug_schedule(cg, mc, sms, maxc, stream_k, M, N, K, L, int(streamout),
+                                    None, 0, ctypes.byref(n), plan)
+    assert rc == gemm_ws.OK
+    rows = np.zeros((max(n.value, 1), 15), dtype=np.int32)
+    rc = lib.gemm_ws_debug_schedule(cg, mc, sms, maxc, stream_k, M, N, K, L, int(streamout),
+                                    rows.ctypes.data, n.value, ctypes.byref(n), plan)
+    assert rc == gemm_ws.OK
+    return list(plan), rows[:n.value]
+
+
+def check(plan, rows, dev, M, N, K, L):
+    cg, mc, sms, maxc = dev
+    cs, clusters, id_bound, T, ns, sk_first, sk_clusters, tm, tn = plan
+    ksub = 1 if cg == 1 else 2
+    assert cs == cg * (mc if cg == 2 else 1)
+    assert tm == -(-M // (BM * cs)) and tn == -(-N // BN) and T == L * tm * tn
+    assert ns == -(-(-(-K // BK)) // ksub)
+    assert 1 <= clusters <= maxc
+    cols = ("c", "i", "id", "tile", "mb", "n0", "width", "l", "kb0", "kb1", "piece", "pieces",
+            "sk_tile", "first", "slot")
+    R = {k: rows[:, j] for j, k in enumerate(cols)}
+
+    # each tile has one (m block, n block, batch), and together they are all of them
+    where = {}
+    for t, mb, n0, l in zip(R["tile"], R["mb"], R["n0"], R["l"]):
+        key = (int(mb), int(n0) // BN, int(l))
+        assert where.setdefault(int(t), key) == key
+        assert 0 <= key[0] < tm and 0 <= key[1] < tn and 0 <= key[2] < L
+    assert sorted(where) == list(range(T)) and len(set(where.values())) == T
+
+    # every stage of every half tile exactly once
+    cover = np.zeros((T, 2, max(ns, 1)), dtype=np.int32)
+    seen_empty = np.zeros((T, 2), dtype=np.int32)
+    for t, n0, width, kb0, kb1 in zip(R["tile"], R["n0"], R["width"], R["kb0"], R["kb1"]):
+        assert width in (BN, BN // 2)
+        halves = [0, 1] if width == BN else [(int(n0) % BN) // (BN // 2)]
+        assert 0 <= kb0 <= kb1 <= ns
+        for h in halves:
+            if ns == 0:
+                seen_empty[t, h] += 1
+            cover[t, h, kb0:kb1] += 1
+    if ns == 0:
+        assert np.all(seen_empty == 1)
+    else:
+        assert np.all(cover == 1)
+
+    # walk order, ids
+    for c in range(clusters):
+        mine = R["i"][R["c"] == c]
+        assert list(mine) == list(range(len(mine)))
+    assert len(set(R["id"].tolist())) == len(rows)
+    assert R["id"].min() >= 0 and R["id"].max() < id_bound
+
+    # stream-K pieces
+    split = R["pieces"] > 1
+    assert np.all(R["slot"][~split] == -1)
+    if sk_first == T:
+        assert not split.any()
+        return
+    assert sk_first % clusters == 0
+    assert np.all(R["tile"][split] >= sk_first)
+    assert np.all(R["sk_tile"][split] == R["tile"][split] - sk_first)
+    slots = R["slot"][split]
+    assert len(set(slots.tolist())) == len(slots)
+    assert slots.min() >= 0 and (slots.max() + 1) * cs <= 3 * sms          # partial parts
+    assert (R["sk_tile"][split].max() + 1) * cs * 32 <= 2 * sms * 32      # chunk counters
+    for t in np.unique(R["tile"][split]):
+        sel = R["tile"] == t
+        n_p = R["pieces"][sel]
+        assert np.all(n_p == n_p[0]) and np.all(R["first"][sel] == R["first"][sel][0])
+        order = np.argsort(R["piece"][sel])
+        assert list(R["piece"][sel][order]) == list(range(n_p[0]))
+        assert list(R["c"][sel][order]) == list(range(R["first"][sel][0],
+                                                      R["first"][sel][0] + n_p[0]))
+        kb0, kb1 = R["kb0"][sel][order], R["kb1"][sel][order]
+        assert kb0[0] == 0 and kb1[-1] == ns and np.all(kb1[:-1] == kb0[1:])
+    # shares: at most three pieces each, equal within one stage
+    in_sk = R["tile"] >= sk_first
+    work = np.zeros(clusters, dtype=np.int64)
+    pieces = np.zeros(clusters, dtype=np.int64)
+    for c, kb0, kb1 in zip(R["c"][in_sk], R["kb0"][in_sk], R["kb1"][in_sk]):
+        work[c] += kb1 - kb0
+        pieces[c] += 1
+    assert pieces.max() <= 3
+    active = work[:sk_clusters]
+    assert active.max() - active.min() <= 1 and np.all(work[sk_clusters:] == 0)
+
+
+@pytest.mark.parametrize("dev", DEVICES, ids=DEVICE_IDS)
+@pytest.mark.parametrize("stream_k", [0, 1, 2], ids=["sk_off", "sk_auto", "sk_always"])
+def test_schedule_covers_every_stage_once(lib, dev, stream_k):
+    for (M, N, K, L) in SHAPES:
+        plan, rows = schedule(lib, dev, stream_k, M, N, K, L)
+        check(plan, rows, dev, M, N, K, L)
+        if stream_k == 0:
+            assert plan[5] == plan[3], (M, N, K, L)
+
+
+@pytest.mark.parametrize("dev", DEVICES, ids=DEVICE_IDS)
+def test_streamout_never_uses_stream_k(lib, dev):
+    for (M, N, K, L) in SHAPES:
+        plan, rows = schedule(lib, dev, 2, M, N, K, L, streamout=True)
+        check(plan, rows, dev, M, N, K, L)
+        assert plan[5] == plan[3]
+
+
+def test_stream_k_where_expected(lib):
+    dev = DEVICES[0]
+    sk = lambda *s: (lambda p: p[3] - p[5])(schedule(lib, dev, 1, *s)[0])
+    assert sk(1024, 1024, 32768, 1) == 16      # few tiles, long K: every tile
+    assert sk(256, 256, 8192, 1) == 1
+    assert sk(2048, 2048, 16384, 1) == 0       # one partial wave: whole tiles by default
+    assert sk(1024, 1024, 1024, 1) == 0        # short K: pieces would be too small
+    assert sk(256, 256, 0, 1) == 0
+    # 152 tiles = exactly two waves of 76 clusters: nothing to balance
+    plan, _ = schedule(lib, dev, 2, 76 * 256 * 2, 256, 4096, 1)
+    assert plan[3] == 152 and plan[5] == 152
