@@ -49,6 +49,7 @@ struct gemm_ws {
 #ifdef GEMM_WS_DEBUG
   int debug_fault;
   unsigned long long* trace;
+  unsigned long long* phases;
 #endif
 };
 
@@ -133,8 +134,9 @@ int check_problem(gemm_ws* h, const uint16_t* A, const uint16_t* B, const uint16
 
 // How many of the last tiles (in raster order) to run as two half-width
 // units so that the persistent schedule's final wave is not half idle.
-// Cluster c runs units c, c + P, ...; a whole tile costs 1, a half ~0.6 (same
-// k-loop and A traffic, half the MMA work). Returns the number of whole
+// Cluster c runs units c, c + P, ...; a whole tile costs 1, a half ~0.8
+// (same k-loop and A traffic, half the MMA work: load-bound; 0.79 measured on
+// GB300 at 4096^3). Returns the number of whole
 // tiles (and, in *cost, the slowest cluster's work in tile units); only
 // splits of at most one wave of tiles are considered (with fewer tiles than
 // clusters, splitting spreads a small problem over more SMs).
@@ -151,7 +153,7 @@ int64_t choose_num_full(int64_t tiles, int64_t P, double* cost) {
     const int64_t F = tiles - s, U = F + 2 * s;
     const int64_t n_full = (F + P - 1) / P, n_units = (U + P - 1) / P;
     const double worst =
-        static_cast<double>(n_full) + 0.6 * static_cast<double>(n_units - n_full);
+        static_cast<double>(n_full) + 0.8 * static_cast<double>(n_units - n_full);
     if (s == 0 || worst < best - 1e-9) {
       best = worst;
       best_full = F;
@@ -207,28 +209,36 @@ int64_t cluster_capacity(const gemm_ws* h, int cs) {
   return cs == 1 ? h->num_sms : (cs == 2 ? h->max_pair_clusters : h->max_quad_clusters);
 }
 
-// Stream-K. The tiles of a stream-K region pool their ring stages and
-// clusters take equal contiguous shares, cut at tile edges into pieces; a
-// tile computed by several pieces gets its fp32 partials summed, per 32 x 32
-// chunk, by the piece that writes that chunk last.
-//  - Default (GEMM_WS_STREAM_K=1): only problems with no more tiles than
-//    half the clusters, as split-K: every tile's K range is cut into S equal
-//    pieces of >= kMinShareK (S <= kMaxSplit), one per cluster, so pieces
-//    with the same index start at the same k on every tile and share their
-//    A and B panels through L2. Used where the host cost model (in
-//    tile-times of the slowest cluster; kPieceCostStages per piece edge for
-//    the partial write, the reduction and the pipeline restart) beats whole
-//    tiles with split halves.
-//  - GEMM_WS_STREAM_K=2 (tests, and callers who measured a gain): also
-//    uneven shares over all clusters, and, with more tiles than clusters, a
-//    stream-K region made of the last partial wave (plus one full wave if it
-//    is under half full) after whole-tile waves. Measured slower than whole
-//    tiles on every such shape tried on GB300: staggered k positions break
-//    the L2 sharing of A and B panels between concurrent tiles, and short
-//    pieces leave the MMA waiting for the epilogue.
+// Stream-K pieces. The tiles of a stream-K region (the last tiles in raster
+// order) have their K ranges cut into S equal pieces, each run by its own
+// cluster as that cluster's last unit; pieces with the same index sit at the
+// same k on every tile, so concurrent tiles still share A and B panels
+// through L2. The 32 x 32 chunks of a tile are owned round-robin by its
+// pieces; the other pieces park fp32 partials of a chunk in the workspace
+// and the owner adds them to its own accumulator, waiting (bounded) until
+// they are there. Because every piece is its cluster's last unit, nothing a
+// piece waits for can itself be waiting: the waits end as soon as all
+// clusters of the launch are resident.
+//  - Few tiles (at most half as many as clusters): every tile, S =
+//    min(clusters / tiles, K / kMinShareK, kMaxSplit) (split-K).
+//  - Otherwise the tiles of the last, partial wave if it is at most half
+//    full: S = min(clusters / those tiles, ...) and the waves before it run
+//    whole tiles (instead of running that wave as half-width tiles, which
+//    cost ~0.8 of a whole one on GB300 because they are load-bound).
+// The default (GEMM_WS_STREAM_K=1) takes the split where the host cost model
+// (tile-times of the slowest cluster; kPieceCostStages of fix-up per piece)
+// beats whole tiles with half-width tails; GEMM_WS_STREAM_K=2 takes it
+// wherever the shape allows, with pieces down to one ring stage (tests).
 constexpr int64_t kMinShareK = 1024;
 constexpr int64_t kMaxSplit = 16;
-constexpr double kPieceCostStages = 4.0;
+constexpr int64_t kMaxSplitForced = 32;   // owner masks in the kernel hold 32 pieces
+// Fix-up of a split tile, measured on GB300 (accumulator complete -> last D
+// store): 7-9 us against ~2 us for a whole tile's epilogue (a chain of L2
+// round trips: partial write, release, count, staged partial reads), plus
+// the pipeline fill of a short piece; at ~0.5-0.6 us per ring stage, ~20
+// stages. With this cost a split is taken only where it measured faster
+// (e.g. not for 4096^3's or 1536^2 x 8192's tail, where half-width tiles win).
+constexpr double kPieceCostStages = 20.0;
 constexpr size_t kPartBytes = size_t{gws::BM} * gws::BN * sizeof(float);
 // One counter per 32 x 32 chunk of a part: 4 lane quarters x 8 subtiles.
 constexpr size_t kCountersPerPart = 4 * gws::SUB_PER_PART;
@@ -275,33 +285,18 @@ Plan make_plan(const gemm_ws* h, int64_t M, int64_t N, int64_t K, int64_t L, boo
   // Stream-out keeps whole tiles: its consumer takes every tile where the
   // epilogue computes it.
   if (streamout || h->stream_k == 0 || !h->partial || P < 2) return q;
-  const int64_t min_share = h->stream_k == 2 ? 1 : kMinShareK / (gws::BK * ksub);
-  if (ns < 2 * min_share) return q;
-  int64_t F, Pe;
-  if (h->stream_k == 1) {
-    if (2 * T > P) return q;
-    int64_t S = P / T;
-    if (S > ns / min_share) S = ns / min_share;
-    if (S > kMaxSplit) S = kMaxSplit;
-    if (S < 2) return q;
-    F = 0;
-    Pe = T * S;
-  } else if (T <= P) {
-    F = 0;
-    Pe = T * ns / min_share;
-    if (Pe > P) Pe = P;
-  } else {
-    const int64_t R = T % P;
-    if (R == 0) return q;
-    F = T - R - (2 * R < P ? P : 0);
-    Pe = P;
-  }
-  const int64_t W = (T - F) * ns;
-  const int64_t share = (W + Pe - 1) / Pe;
-  if (Pe < 2 || share > 2 * ns + 1) return q;   // would touch more than three tiles
-  const double sk_cost = static_cast<double>(F / P) + static_cast<double>(share) / ns +
-                         2.0 * kPieceCostStages / static_cast<double>(ns);
-  if (h->stream_k != 2 && !(sk_cost < dp_cost - 1e-9)) return q;
+  const bool forced = h->stream_k == 2;
+  const int64_t min_share = forced ? 1 : kMinShareK / (gws::BK * ksub);
+  const int64_t R = 2 * T <= P ? T : T % P;   // tiles of the stream-K region
+  if (R == 0 || 2 * R > P) return q;
+  int64_t S = P / R;
+  if (S > ns / min_share) S = ns / min_share;
+  if (S > (forced ? kMaxSplitForced : kMaxSplit)) S = forced ? kMaxSplitForced : kMaxSplit;
+  if (S < 2) return q;
+  const int64_t F = T - R, Pe = R * S, W = R * ns;
+  const double sk_cost = static_cast<double>(F / P) + static_cast<double>((ns + S - 1) / S) / ns +
+                         kPieceCostStages / static_cast<double>(ns);
+  if (!forced && !(sk_cost < dp_cost - 1e-9)) return q;
   q.sk_first = F;
   q.sk_clusters = Pe;
   q.sk_work = W;
@@ -382,6 +377,7 @@ int launch(gemm_ws* h, const uint16_t* A, const uint16_t* B, const uint16_t* C, 
 #ifdef GEMM_WS_DEBUG
   p.debug_fault = h->debug_fault;
   p.trace = h->trace;
+  p.phases = h->phases;
 #endif
 
   cudaError_t e;
@@ -639,6 +635,12 @@ int gemm_ws_debug_configure(gemm_ws_t* h, int fault, unsigned long long* trace) 
   if (!h || fault < 0 || fault > 1) return GEMM_WS_ERR_INVALID_ARG;
   h->debug_fault = fault;
   h->trace = trace;
+  return GEMM_WS_OK;
+}
+
+int gemm_ws_debug_phases(gemm_ws_t* h, unsigned long long* phases) {
+  if (!h) return GEMM_WS_ERR_INVALID_ARG;
+  h->phases = phases;
   return GEMM_WS_OK;
 }
 

@@ -73,6 +73,9 @@ constexpr int EPI_HALF_WARPS = 4;        // one per lane quarter: a half covers 
 constexpr int STAGING = 128;             // stream-out tile edge
 constexpr int SUB_PER_STAGING = STAGING / EPI_N;
 constexpr int SUB_PER_PART = BN / EPI_N;   // subtiles (32 x 32 chunks per lane quarter) of a part
+constexpr int CHUNK_BYTES = 32 * EPI_N * 4;  // one 32 x 32 fp32 partial chunk
+constexpr int RED_BATCH = 6;                 // partial chunks staged at once per epilogue warp
+constexpr uint32_t RED_AREA_BYTES = RED_BATCH * CHUNK_BYTES;
 static_assert(SUB_PER_PART == 8, "split-K chunk rotation assumes four subtiles per epilogue warp");
 constexpr int WARP_TMA = 0;
 constexpr int WARP_MMA = 1;
@@ -136,6 +139,8 @@ struct Cfg {
   static constexpr uint32_t IDESC = idesc_bf16_f32(TILE_M, BN);
   static constexpr uint32_t IDESC_HALF = idesc_bf16_f32(TILE_M, BN / 2);
   static_assert(STAGES <= NUM_STAGES_MAX, "barrier table");
+  static_assert(OFF_B + STAGES * B_STAGE_BYTES - OFF_A >= NUM_EPI_WARPS * RED_AREA_BYTES,
+                "the split-K reduction stages partials in the operand ring");
   static_assert(SMEM_BYTES <= 232448, "exceeds the 227 KiB per-CTA shared memory");
   static_assert(OFF_B % 1024 == 0 && OFF_D % 1024 == 0 && OFF_C % 1024 == 0, "alignment");
 };
@@ -175,6 +180,7 @@ struct Params {
 #ifdef GEMM_WS_DEBUG
   int debug_fault;               // 1: the stream-out consumer takes no tile
   unsigned long long* trace;     // [tile][CG][2] global-timer stamps, or null
+  unsigned long long* phases;    // [CTA][8] stamps (see gemm_ws_debug_phases), or null
 #endif
 };
 
@@ -383,6 +389,23 @@ template <bool kCluster>
 __device__ __forceinline__ bool wait_spin(uint32_t bar, uint32_t parity, const Watchdog& wd) {
   if (kCluster ? mbar_test_wait_cluster(bar, parity) : mbar_test_wait(bar, parity)) return true;
   return spin_slow<kCluster>(bar, parity, wd);
+}
+
+// Bounded wait (one thread) until a global counter reaches `target`, with
+// acquire semantics. Returns false if the CTA is aborting or the wait
+// exceeded the limit (which then starts the abort).
+__device__ __noinline__ bool wait_count(const uint32_t* cnt, uint32_t target, const Watchdog& wd) {
+  if (ld_acquire_gpu(cnt) >= target) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (;;) {
+    if (ld_acquire_gpu(cnt) >= target) return true;
+    if (*wd.abort) return false;
+    if (global_timer_ns() - t0 > wd.limit_ns) {
+      *wd.abort = 1;
+      atomicExch(wd.status, STATUS_TIMEOUT);
+      return false;
+    }
+  }
 }
 
 // Short bounded wait used only while draining after an abort.
@@ -745,25 +768,39 @@ __device__ __forceinline__ void epilogue_role(const Params& p, uint32_t sbase, u
         }
       }
     } else {
-      // A piece of the tile's K range. The warp's four 32 x 32 chunks (its TMEM lane quarter q,
-      // subtiles j = hf, hf+2, ...) each go to the workspace in the TMEM
-      // register layout: float4 c of lane r at [c][r], so a warp's store or
-      // load is 512 contiguous bytes. Each chunk has its own arrival
-      // counter; the piece whose write completes the count adds the S
-      // partials of that chunk (in piece order: the bits do not depend on
-      // which piece it is) and runs the epilogue for it (the fixup /
-      // compute_epilogue step of the SM90 cooperative kernel). Pieces start at
-      // different chunks, so when they finish together the chunks' last
-      // writers, and the reductions, spread over the pieces. Nothing waits
-      // for another CTA.
+      // A piece of the tile's K range (every piece of a tile runs on its own
+      // cluster, as that cluster's last unit). Each of the warp's four 32 x 32
+      // chunks (TMEM lane quarter q, subtiles j = hf + 2k) has an owner piece;
+      // the others park their fp32 partial of it in the workspace (TMEM
+      // register order: float4 c of lane r at [c][r], so a warp's store or
+      // load is 512 contiguous bytes) and count in on the warp's chunk-group
+      // counter with a release add. The owner waits (bounded) for all pieces
+      // to count in, adds the partials to its own accumulator in piece order
+      // (so the bits do not depend on which piece owns the chunk) and runs
+      // the epilogue for the chunk: the fixup / compute_epilogue step of the
+      // SM90 cooperative kernel. Owners are spread round-robin over the
+      // pieces, so the reduction is shared by all of them.
+      const int S = w.pieces;
       auto chunk_of = [&](int piece, int j) -> float* {
         const size_t part = static_cast<size_t>(sk_slot(p, w, piece)) * C::CS + rank;
         return p.partial + ((part * 4 + q) * SUB_PER_PART + j) * (32 * EPI_N);
       };
-      uint32_t mine = 0;   // bit j: this piece completed chunk j's count
-      for (int i = 0; i < SUB_PER_PART / 2; ++i) {
-        const int j = hf + 2 * ((i + w.piece) & (SUB_PER_PART / 2 - 1));
-        if (j >= nsub) continue;   // outside N (or this CTA's rows outside M)
+      auto owner = [&](int k) { return (e * (SUB_PER_PART / 2) + k) % S; };
+      uint32_t* cnt = p.split_count + ((static_cast<size_t>(w.sk_tile) * C::CS + rank) *
+                                           NUM_EPI_WARPS + e) * 2;
+      uint32_t own = 0;      // bit k: this piece owns chunk k (inside N)
+      uint32_t owners = 0;   // bit o: piece o owns a chunk of this warp (o < 32)
+      int valid = 0;
+      for (int k = 0; k < SUB_PER_PART / 2; ++k) {
+        if (hf + 2 * k >= nsub) continue;   // outside N (or this CTA's rows outside M)
+        ++valid;
+        owners |= 1u << (owner(k) & 31);
+        if (owner(k) == w.piece) own |= 1u << k;
+      }
+      // 1) The partials of the chunks other pieces own.
+      for (int k = 0; k < SUB_PER_PART / 2; ++k) {
+        const int j = hf + 2 * k;
+        if (j >= nsub || (own >> k) & 1u) continue;
         uint32_t acc[32];
         tmem_ld_32x32b_x32(tacc + j * EPI_N, acc);
         tmem_wait_ld();
@@ -773,73 +810,116 @@ __device__ __forceinline__ void epilogue_role(const Params& p, uint32_t sbase, u
           __stcg(dst + c * 32 + lane,
                  make_float4(__uint_as_float(acc[4 * c]), __uint_as_float(acc[4 * c + 1]),
                              __uint_as_float(acc[4 * c + 2]), __uint_as_float(acc[4 * c + 3])));
-        fence_acq_rel_gpu();   // this lane's partial before the count (the warp syncs below)
-        __syncwarp();
-        uint32_t last = 0;
-        if (lane == 0) {
-          uint32_t* cnt = p.split_count +
-                          ((static_cast<size_t>(w.sk_tile) * C::CS + rank) * 4 + q) * SUB_PER_PART + j;
-          last = atomicAdd(cnt, 1u) == static_cast<uint32_t>(w.pieces - 1) ? 1u : 0u;
-          if (last) atomicExch(cnt, 0u);   // all pieces in: ready for the next launch
-        }
-        mine |= __shfl_sync(0xffffffffu, last, 0) << j;
       }
-      release_acc();
-      if (mine) fence_acq_rel_gpu();   // the other pieces' partials, counted in before ours
-      // Chunks to finish, in increasing j; the C load of the first goes out now.
-      int j = mine ? __ffs(mine) - 1 : -1;
-      if (p.has_c && j >= 0) issue_c(j);
-      while (j >= 0) {
-        const uint32_t rest = mine & ~((2u << j) - 1u);
-        const int next = rest ? __ffs(rest) - 1 : -1;
-        float v[32];
-#pragma unroll
-        for (int x = 0; x < 32; ++x) v[x] = 0.0f;
-        int sk = 0;
-        for (; sk + 1 < w.pieces; sk += 2) {
-          const float4* s0 = reinterpret_cast<const float4*>(chunk_of(sk, j)) + lane;
-          const float4* s1 = reinterpret_cast<const float4*>(chunk_of(sk + 1, j)) + lane;
-          float4 f0[8], f1[8];
-#pragma unroll
-          for (int c = 0; c < 8; ++c) f0[c] = __ldcg(s0 + c * 32);   // L2: other SMs wrote it
-#pragma unroll
-          for (int c = 0; c < 8; ++c) f1[c] = __ldcg(s1 + c * 32);
-#pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            v[4 * c] += f0[c].x;
-            v[4 * c + 1] += f0[c].y;
-            v[4 * c + 2] += f0[c].z;
-            v[4 * c + 3] += f0[c].w;
-          }
-#pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            v[4 * c] += f1[c].x;
-            v[4 * c + 1] += f1[c].y;
-            v[4 * c + 2] += f1[c].z;
-            v[4 * c + 3] += f1[c].w;
-          }
-        }
-        if (sk < w.pieces) {
-          const float4* s0 = reinterpret_cast<const float4*>(chunk_of(sk, j)) + lane;
-#pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            const float4 f = __ldcg(s0 + c * 32);
-            v[4 * c] += f.x;
-            v[4 * c + 1] += f.y;
-            v[4 * c + 2] += f.z;
-            v[4 * c + 3] += f.w;
-          }
-        }
-#pragma unroll
-        for (int x = 0; x < 32; ++x) v[x] *= p.alpha;
-        if (!finish_subtile(j, v, next)) {
-          ok = false;
+#ifdef GEMM_WS_DEBUG
+      if (p.phases && e == 0 && lane == 0) p.phases[blockIdx.x * 8 + 3] = global_timer_ns();
+#endif
+      if (valid > 0) {
+        fence_acq_rel_gpu();   // this lane's partials before the count (the warp syncs below)
+        __syncwarp();
+        if (lane == 0) red_release_gpu_add(cnt, 1u);
+      }
+#ifdef GEMM_WS_DEBUG
+      if (p.phases && e == 0 && lane == 0) p.phases[blockIdx.x * 8 + 4] = global_timer_ns();
+#endif
+      if (own == 0) {
+        release_acc();
+      } else {
+        // 2) Every piece has counted in: its partials of this warp's chunks are there.
+        uint32_t in = 0;
+        if (lane == 0) in = wait_count(cnt, static_cast<uint32_t>(S), wd) ? 1u : 0u;
+        in = __shfl_sync(0xffffffffu, in, 0);
+        if (!in) {
+          release_acc();
           break;
         }
-        j = next;
+        fence_acq_rel_gpu();   // acquire, for every lane, the partials counted in
+#ifdef GEMM_WS_DEBUG
+        if (p.phases && e == 0 && lane == 0) p.phases[blockIdx.x * 8 + 5] = global_timer_ns();
+#endif
+
+        // 3) The owned chunks: own accumulator plus the other pieces' partials.
+        const uint32_t area = sbase + C::OFF_A + static_cast<uint32_t>(e) * RED_AREA_BYTES;
+        int k = __ffs(own) - 1;
+        if (p.has_c) issue_c(hf + 2 * k);
+        while (k >= 0) {
+          const int j = hf + 2 * k;
+          const uint32_t rest = own & ~((2u << k) - 1u);
+          const int next = rest ? __ffs(rest) - 1 : -1;
+          float v[32];
+#pragma unroll
+          for (int x = 0; x < 32; ++x) v[x] = 0.0f;
+          // Sum in piece order, this piece's own part straight from TMEM at
+          // its place. The other pieces' partials come in batches of up to
+          // RED_BATCH through the warp's share of the operand ring (idle: this
+          // is the cluster's last unit and its MMAs are done): every lane
+          // copies its own 16-byte pieces with cp.async, a batch in flight at
+          // once, then reads back only what it copied. (One batch for all
+          // pieces, in a larger share of the ring, measured slower.)
+          for (int pc = 0; pc < S;) {
+            int n = 0, end = pc;
+            for (; end < S && n < RED_BATCH; ++end)
+              if (end != w.piece) ++n;
+            int b2 = 0;
+            for (int pb = pc; pb < end; ++pb) {
+              if (pb == w.piece) continue;
+              const float4* src = reinterpret_cast<const float4*>(chunk_of(pb, j)) + lane;
+#pragma unroll
+              for (int c = 0; c < 8; ++c)
+                cp_async_16(area + b2 * CHUNK_BYTES + (c * 32 + lane) * 16, src + c * 32);
+              ++b2;
+            }
+            cp_async_wait_all();
+            for (b2 = 0; pc < end; ++pc) {
+              if (pc == w.piece) {
+                uint32_t acc[32];
+                tmem_ld_32x32b_x32(tacc + j * EPI_N, acc);
+                tmem_wait_ld();
+#pragma unroll
+                for (int x = 0; x < 32; ++x) v[x] += __uint_as_float(acc[x]);
+                continue;
+              }
+              const float4* sp4 =
+                  reinterpret_cast<const float4*>(smem + (area - sbase) + b2 * CHUNK_BYTES) + lane;
+#pragma unroll
+              for (int c = 0; c < 8; ++c) {
+                const float4 f = sp4[c * 32];
+                v[4 * c] += f.x;
+                v[4 * c + 1] += f.y;
+                v[4 * c + 2] += f.z;
+                v[4 * c + 3] += f.w;
+              }
+              ++b2;
+            }
+          }
+          if (next < 0) release_acc();   // every TMEM read of this unit is done
+#pragma unroll
+          for (int x = 0; x < 32; ++x) v[x] *= p.alpha;
+          if (!finish_subtile(j, v, next >= 0 ? hf + 2 * next : -1)) {
+            ok = false;
+            break;
+          }
+          k = next;
+        }
+#ifdef GEMM_WS_DEBUG
+        if (p.phases && e == 0 && lane == 0) p.phases[blockIdx.x * 8 + 6] = global_timer_ns();
+#endif
+        // 4) The last owner to finish returns the warp's counters to zero.
+        if (ok && lane == 0) {
+          const uint32_t n_owners = static_cast<uint32_t>(__popc(owners));
+          if (atomicAdd(cnt + 1, 1u) == n_owners - 1) {
+            atomicExch(cnt, 0u);
+            atomicExch(cnt + 1, 0u);
+          }
+        }
       }
     }
     if (!ok) break;
+#ifdef GEMM_WS_DEBUG
+    // stamp 1 without stream-out: this warp issued the part's last D store
+    if (p.trace && !p.streamout && q == (WARP_EPI0 & 3) && hf == 0 && lane == 0)
+      p.trace[(static_cast<size_t>(w.id) * C::CS + rank) * 2 + 1] = global_timer_ns();
+#endif
   }
   if (lane == 0) {
     // A C load still in flight only after an abort: let it land first.
@@ -938,6 +1018,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_ws_kernel(const __grid_co
   const uint32_t rank = C::CS == 1 ? 0u : cluster_ctarank();
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + C::OFF_ABORT);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_TMEM_SLOT);
+#ifdef GEMM_WS_DEBUG
+  unsigned long long t_entry = 0;
+  if (p.phases && threadIdx.x == 0) t_entry = global_timer_ns();
+#endif
 
   if (warp == WARP_TMA && lane == 0) {
     auto bar = [&](int i) { return sbase + C::OFF_BAR + 8 * i; };
@@ -987,6 +1071,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_ws_kernel(const __grid_co
   // (its CTAs take SMs as this grid's CTAs leave them).
   grid_dependency_wait();
   if (threadIdx.x == 0) grid_launch_dependents();
+#ifdef GEMM_WS_DEBUG
+  // Stamps per CTA: entry, start of work (after the previous grid), exit.
+  if (p.phases && threadIdx.x == 0) {
+    p.phases[blockIdx.x * 8] = t_entry;
+    p.phases[blockIdx.x * 8 + 1] = global_timer_ns();
+  }
+#endif
 
   if (warp == WARP_TMA || warp == WARP_TMA_B) {
     if (lane == 0)
@@ -1012,6 +1103,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_ws_kernel(const __grid_co
     else
       tmem_dealloc_pair(tmem_base, TMEM_COLS);
   }
+#ifdef GEMM_WS_DEBUG
+  if (p.phases && threadIdx.x == 0) p.phases[blockIdx.x * 8 + 2] = global_timer_ns();
+#endif
 }
 
 }  // namespace gws

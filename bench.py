@@ -39,6 +39,8 @@ METRIC = ("bf16 GEMM TFLOP/s & % of GB300 dense bf16 peak (8192³); "
 UNIT = "TFLOP/s"
 NOMINAL_BF16_TFLOPS = 2250.0
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# Timed regions at least this long are compared with the sustained peak.
+SUSTAINED_MIN_S = 0.25
 KERNEL_SOURCES = ["async_pipelines_gb300/csrc/gemm_ws.cu",
                   "async_pipelines_gb300/csrc/gemm_ws_kernel.cuh",
                   "async_pipelines_gb300/csrc/ptx.cuh"]
@@ -403,6 +405,14 @@ def run_ours(args, rank, world, local):
         return
     peaks, peak_src = load_peaks()
     peak = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
+    peak_sus = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
+    # The roofline denominator matches how the kernel was timed: launches
+    # back to back for a quarter of a second or more run in the power-capped
+    # regime of the sustained library measurement (a seconds-long loop);
+    # shorter timed regions compare with the burst figure.
+    timed_s = ms * args.steps / 1e3
+    regime = "sustained" if timed_s >= SUSTAINED_MIN_S else "burst"
+    roof_peak = peak_sus if regime == "sustained" else peak
     cpu = None
     if not args.no_cpu_baseline:
         sampler = OracleSampler(w)
@@ -441,9 +451,11 @@ def run_ours(args, rank, world, local):
         "gpu_launches": args.steps,
         "pct_of_measured_bf16_sustained": round(
             100.0 * tflops_rank / peaks.get("bf16_tflops_sustained", peak), 2),
-        "roofline": {"bound": "tensor", "achieved": round(tflops_rank, 2), "peak": peak,
-                     "unit": "TFLOP/s", "frac": round(tflops_rank / peak, 4),
-                     "peak_source": f"{peak_src} bf16 burst (cuBLAS 8192^3)",
+        "roofline": {"bound": "tensor", "achieved": round(tflops_rank, 2), "peak": roof_peak,
+                     "unit": "TFLOP/s", "frac": round(tflops_rank / roof_peak, 4),
+                     "peak_source": f"{peak_src} bf16 {regime} (cuBLAS 8192^3); timed region "
+                                    f"{timed_s:.2f} s of back-to-back launches",
+                     "frac_of_burst": round(tflops_rank / peak, 4),
                      "traffic": traffic_for(w.name),
                      "algorithmic_bytes_per_launch": w.algorithmic_bytes(),
                      "kernel": "gws::gemm_ws_kernel"},

@@ -26,8 +26,9 @@
  * Ownership: every data pointer is a borrowed DEVICE pointer on the handle's
  * device; the caller owns it and keeps it alive until the stream work ends.
  * The handle owns only its device workspace: the stream-out sequence
- * counter, a status word, a completion count, and the split-K area (three
- * 128 x 256 fp32 partials and 64 chunk counters per SM, ~384 KiB per SM).
+ * counter, a status word, a completion count, and the split-K area (up to
+ * three 128 x 256 fp32 partials and 64 counter words per SM, ~384 KiB per
+ * SM).
  * The kernel returns every counter to zero before it ends, so runs need no
  * clearing between them; runs on one handle that overlap on the GPU (e.g. on
  * two streams) race on that workspace: serialise them or use one handle per
@@ -80,15 +81,17 @@ int gemm_ws_destroy(gemm_ws_t* h);
  *  - K == 0 gives D = beta * C (or 0); M*N*L == 0 launches nothing.
  *  - D must not overlap A or B; D may be exactly C (in place).
  * Rounding: fp32 alpha * acc + beta * c, then round-to-nearest-even to bf16.
- * Split-K (stream-K pieces): when the output has at most half as many
- * tiles as the GPU has persistent clusters and K >= 2048, each tile's K
- * range is cut into 2..16 equal pieces of >= 1024 that run on separate
- * clusters; acc is then the sum, in piece order, of the pieces' fp32
- * partials (deterministic: the same bits on every run). GEMM_WS_STREAM_K in
- * the environment at gemm_ws_create sets this per handle: 0 off, 1 (default)
- * as described, 2 stream-K wherever the schedule allows it (uneven shares
- * over all clusters, and a stream-K region after whole-tile waves).
- * gemm_ws_run_streamout never splits. */
+ * Split-K / stream-K pieces: when the output has at most half as many tiles
+ * as the GPU has persistent clusters and K is long, or the last wave of
+ * tiles is at most half full, those tiles' K ranges may be cut into 2..16
+ * equal pieces of >= 1024 that run on separate clusters (chosen by a host
+ * cost model); acc is then the sum, in piece order, of the pieces' fp32
+ * partials (deterministic: the same bits on every run). The pieces of a tile
+ * wait for each other (bounded by the watchdog), which needs every cluster
+ * of the launch resident at once, as on a whole, unshared GPU.
+ * GEMM_WS_STREAM_K in the environment at gemm_ws_create sets this per
+ * handle: 0 off, 1 (default) by the cost model, 2 wherever the shape allows
+ * (pieces down to one ring stage). gemm_ws_run_streamout never splits. */
 int gemm_ws_run(gemm_ws_t* h, const uint16_t* A, const uint16_t* B,
                 const uint16_t* C, uint16_t* D, int64_t M, int64_t N, int64_t K,
                 int64_t L, float alpha, float beta, void* stream);
@@ -116,7 +119,9 @@ int gemm_ws_run_streamout(gemm_ws_t* h, const uint16_t* A, const uint16_t* B,
 
 /* Synchronises `stream` and returns the device status word of the handle:
  * GEMM_WS_OK, or GEMM_WS_ERR_TIMEOUT if a run's bounded wait gave up (the
- * run's outputs are then undefined). Reading clears the word. */
+ * run's outputs are then undefined). Reading a non-zero word clears it and
+ * returns the workspace counters to zero; after a timeout, call this before
+ * the next run on the handle. */
 int gemm_ws_query_status(gemm_ws_t* h, void* stream);
 
 /* The last CUDA error code (cudaError_t value) seen by this handle, 0 if none. */

@@ -30,11 +30,24 @@ extern "C" {
  *    gemm_ws_debug_launch_shape) or NULL. For work unit u and CTA rank r
  *    in its cluster, trace[(u*ctas_per_cluster + r)*2] = global time (ns) at which
  *    that CTA's epilogue saw the unit's accumulator complete, and [...+1] =
- *    time at which its consumer published the last stream-out tile of that
- *    part (written only by gemm_ws_run_streamout; untouched where the part
- *    lies outside M x N). The caller owns the buffer.
+ *    with gemm_ws_run_streamout, time at which its consumer published the
+ *    last stream-out tile of that part (untouched where the part lies
+ *    outside M x N); with gemm_ws_run, time at which one epilogue warp (of
+ *    the first lane quarter's even subtiles) issued its last D store of the
+ *    unit. The caller owns the buffer.
  * Returns GEMM_WS_OK or GEMM_WS_ERR_INVALID_ARG. */
 int gemm_ws_debug_configure(gemm_ws_t* h, int fault, unsigned long long* trace);
+
+/* Sets (or, with NULL, clears) a device buffer of 8 uint64 per CTA of the
+ * handle's later launches (size it with gemm_ws_debug_launch_shape:
+ * clusters * ctas_per_cluster CTAs): for CTA b, phases[8b] = global time
+ * (ns) at kernel entry, [8b+1] = after the wait for the previous grid in
+ * the stream, [8b+2] = at exit; for the CTA's last split piece, as seen by
+ * its first epilogue warp: [8b+3] partials written, [8b+4] counted in,
+ * [8b+5] all pieces counted in (owners only), [8b+6] owned chunks stored
+ * (owners only). Slots not reached stay as the caller left them. The
+ * caller owns the buffer. Returns GEMM_WS_OK or GEMM_WS_ERR_INVALID_ARG. */
+int gemm_ws_debug_phases(gemm_ws_t* h, unsigned long long* phases);
 
 /* The launch the handle would make for an M x N x K x L problem (streamout:
  * nonzero for gemm_ws_run_streamout, 0 for gemm_ws_run): CTAs per cluster

@@ -11,8 +11,8 @@ many problem shapes, device shapes and stream-K settings, that
 - every workspace slot and chunk-counter index stays inside the buffers the
   handle allocates (3 partial parts and 2 counter sets per SM), slots are
   never shared, and unit ids are unique and below the reported bound;
-- no cluster walks more than three stream-K pieces and the stream-K shares
-  differ by at most one stage;
+- every cluster runs at most one piece, as its last unit, all pieces are
+  equal within one stage, and piece s of every tile starts at the same k;
 - stream-out and GEMM_WS_STREAM_K=0 plans never use stream-K.
 """
 from __future__ import annotations
@@ -129,16 +129,23 @@ def check(plan, rows, dev, M, N, K, L):
                                                       R["first"][sel][0] + n_p[0]))
         kb0, kb1 = R["kb0"][sel][order], R["kb1"][sel][order]
         assert kb0[0] == 0 and kb1[-1] == ns and np.all(kb1[:-1] == kb0[1:])
-    # shares: at most three pieces each, equal within one stage
+    # one piece per cluster, as its last unit; all tiles of the region split
+    # the same number of ways into pieces equal within one stage, with piece
+    # s of every tile starting at the same k
     in_sk = R["tile"] >= sk_first
-    work = np.zeros(clusters, dtype=np.int64)
-    pieces = np.zeros(clusters, dtype=np.int64)
-    for c, kb0, kb1 in zip(R["c"][in_sk], R["kb0"][in_sk], R["kb1"][in_sk]):
-        work[c] += kb1 - kb0
-        pieces[c] += 1
-    assert pieces.max() <= 3
-    active = work[:sk_clusters]
-    assert active.max() - active.min() <= 1 and np.all(work[sk_clusters:] == 0)
+    assert np.all(split == in_sk)
+    for c in np.unique(R["c"][in_sk]):
+        mine = R["c"] == c
+        assert (mine & in_sk).sum() == 1
+        assert R["i"][mine & in_sk][0] == R["i"][mine].max()
+    assert len(set(R["pieces"][in_sk].tolist())) == 1
+    S = int(R["pieces"][in_sk][0])
+    assert 2 <= S <= 32 and sk_clusters == (T - sk_first) * S
+    length = R["kb1"][in_sk] - R["kb0"][in_sk]
+    assert length.max() - length.min() <= 1
+    starts = {}
+    for piece, kb0 in zip(R["piece"][in_sk], R["kb0"][in_sk]):
+        assert starts.setdefault(int(piece), int(kb0)) == kb0
 
 
 @pytest.mark.parametrize("dev", DEVICES, ids=DEVICE_IDS)
@@ -164,7 +171,10 @@ def test_stream_k_where_expected(lib):
     sk = lambda *s: (lambda p: p[3] - p[5])(schedule(lib, dev, 1, *s)[0])
     assert sk(1024, 1024, 32768, 1) == 16      # few tiles, long K: every tile
     assert sk(256, 256, 8192, 1) == 1
-    assert sk(2048, 2048, 16384, 1) == 0       # one partial wave: whole tiles by default
+    assert sk(2048, 2048, 16384, 1) == 0       # one partial wave, over half full: whole tiles
+    assert sk(4096, 4096, 4096, 1) == 0        # 256 = 3 * 76 + 28: half-width tail is cheaper
+    assert sk(8192, 8192, 8192, 1) == 0        # 1024 = 13 * 76 + 36: no measured gain
+    assert sk(1536, 1536, 8192, 1) == 0        # 36 tiles: half-width tiles measured faster
     assert sk(1024, 1024, 1024, 1) == 0        # short K: pieces would be too small
     assert sk(256, 256, 0, 1) == 0
     # 152 tiles = exactly two waves of 76 clusters: nothing to balance
