@@ -31,7 +31,7 @@ constexpr int kMapCache = 16;
 struct gemm_ws {
   int device;
   int num_sms;
-  int cta_group;                  // 2: CTA-pair tiles (default); 1: single-CTA tiles
+  int cta_group;                  // 0: chosen per problem (default); 1: single-CTA tiles; 2: CTA pairs
   int multicast;                  // 2: two CTA pairs per cluster share B by TMA multicast
   int pdl;                        // launch with programmatic stream serialisation
   int max_quad_clusters;          // co-resident 4-CTA clusters of the multicast kernel
@@ -250,6 +250,7 @@ constexpr int kScheduleCols = 15;   // columns of a gemm_ws_debug_schedule row
 #endif
 
 struct Plan {
+  int cg;              // CTA group of the MMA (1 or 2)
   int cs;              // CTAs per cluster
   int64_t tiles_m, tiles_n, num_tiles;
   int64_t num_full;    // whole-width units (the rest of the tiles run as halves)
@@ -261,11 +262,28 @@ struct Plan {
   int64_t clusters;    // persistent clusters launched
 };
 
+// Tile configuration of one problem: single-CTA 128 x 256 tiles where the
+// work per tile is short (K <= 512: the epilogue, not the MMA, bounds it) or
+// the problem is small (K <= 1024 with at most two waves of pair tiles), CTA
+// pairs with 256 x 256 tiles otherwise. Measured on GB300 over M = N in
+// 256..8192, K in 64..8192: single CTAs are 16-33 % faster at K <= 256 and
+// up to 14 % at K = 1024 on small problems; pairs 7-18 % faster for K >= 2048
+// on larger ones. The handle can force either (GEMM_WS_CTA_GROUP).
+int pick_cta_group(const gemm_ws* h, int64_t M, int64_t N, int64_t K, int64_t L) {
+  if (h->cta_group == 1 || h->max_pair_clusters < 1) return 1;
+  if (h->cta_group == 2 || h->multicast == 2) return 2;
+  const int64_t pair_tiles = L * ((M + 2 * gws::BM - 1) / (2 * gws::BM)) * ((N + gws::BN - 1) / gws::BN);
+  if (K <= 512 || (K <= 1024 && pair_tiles <= 2 * static_cast<int64_t>(h->max_pair_clusters)))
+    return 1;
+  return 2;
+}
+
 // The persistent schedule of one launch: host arithmetic only, shared by the
 // launch and the debug query.
 Plan make_plan(const gemm_ws* h, int64_t M, int64_t N, int64_t K, int64_t L, bool streamout) {
   Plan q;
-  const int cg = h->cta_group;
+  const int cg = pick_cta_group(h, M, N, K, L);
+  q.cg = cg;
   q.cs = cg * (cg == 2 ? h->multicast : 1);
   q.tiles_m = (M + gws::BM * q.cs - 1) / (gws::BM * q.cs);
   q.tiles_n = (N + gws::BN - 1) / gws::BN;
@@ -311,9 +329,9 @@ int launch(gemm_ws* h, const uint16_t* A, const uint16_t* B, const uint16_t* C, 
            uint16_t* staging, uint32_t* flags, cudaStream_t stream) {
   gws::Params p;
   std::memset(&p, 0, sizeof p);
-  const int cg = h->cta_group;
-  const int mc = cg == 2 ? h->multicast : 1;
   const Plan q = make_plan(h, M, N, K, L, staging != nullptr);
+  const int cg = q.cg;
+  const int mc = cg == 2 ? h->multicast : 1;
   const int cs = q.cs;   // CTAs per cluster
   if (q.num_units > kMaxDim) return GEMM_WS_ERR_INVALID_ARG;
   const int64_t stn = (N + gws::STAGING - 1) / gws::STAGING;
@@ -438,13 +456,14 @@ int pdl_from_env() {
   return 1;
 }
 
-// GEMM_WS_CTA_GROUP=1 selects single-CTA 128 x 256 tiles; the default is
-// CTA-pair 256 x 256 tiles.
+// GEMM_WS_CTA_GROUP=1 forces single-CTA 128 x 256 tiles, =2 CTA-pair
+// 256 x 256 tiles; by default the library picks per problem.
 int cta_group_from_env() {
   if (const char* s = std::getenv("GEMM_WS_CTA_GROUP")) {
-    if (std::atoi(s) == 1) return 1;
+    const int v = std::atoi(s);
+    if (v == 1 || v == 2) return v;
   }
-  return 2;
+  return 0;
 }
 
 // GEMM_WS_STREAM_K: 0 keeps every tile's K range whole; 2 uses stream-K
@@ -527,6 +546,7 @@ int gemm_ws_create(gemm_ws_t** out, int device) {
   e = configure_kernels(h->num_sms, &h->max_pair_clusters, &h->max_quad_clusters);
   if (e == cudaSuccess && h->max_quad_clusters < 1) h->multicast = 1;
   if (e == cudaSuccess && h->max_pair_clusters < 1) h->cta_group = 1;
+  if (e == cudaSuccess && h->multicast == 2 && h->cta_group == 1) h->multicast = 1;
   if (e == cudaSuccess) e = cudaMalloc(&h->work, kWorkWords * sizeof(uint32_t));
   if (e == cudaSuccess) e = cudaMemset(h->work, 0, kWorkWords * sizeof(uint32_t));
   // Stream-K workspace: each cluster runs at most three pieces (one partial

@@ -924,7 +924,10 @@ __device__ __forceinline__ void epilogue_role(const Params& p, uint32_t sbase, u
   if (lane == 0) {
     // A C load still in flight only after an abort: let it land first.
     for (uint32_t idx = cu; idx < c_issued; ++idx) wait_drain(cbar, idx & 1);
-    bulk_wait<0>();   // store tail: every D write has landed
+    // Store tail: the D stores have finished reading shared memory, which
+    // the CTA may release once every role is done. Their global writes are
+    // performed before the grid completes, so nothing waits for them here.
+    bulk_wait_read<0>();
   }
   __syncwarp();
 }
