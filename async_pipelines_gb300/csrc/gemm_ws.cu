@@ -39,8 +39,8 @@ struct gemm_ws {
   int max_pair_clusters;          // co-resident 2-CTA clusters of the pair kernel
   int stream_k;                   // 0 off, 1 where the cost model gains (default), 2 always
   uint32_t* work;                 // [0] stream-out counter, [1] status, [2] done count
-  float* partial;                 // stream-K partials: 3 * num_sms parts of 128 x 256 fp32
-  uint32_t* split_count;          // stream-K chunk counters, 2 * num_sms * 32 words (kept at zero)
+  float* partial;                 // stream-K partials: num_sms parts of 128 x 256 fp32
+  uint32_t* split_count;          // stream-K counters, 16 words per SM (kept at zero)
   int last_cuda_error;
   unsigned long long timeout_ns;
   PFN_cuTensorMapEncodeTiled_v12000 encode;
@@ -240,11 +240,9 @@ constexpr int64_t kMaxSplitForced = 32;   // owner masks in the kernel hold 32 p
 // (e.g. not for 4096^3's or 1536^2 x 8192's tail, where half-width tiles win).
 constexpr double kPieceCostStages = 20.0;
 constexpr size_t kPartBytes = size_t{gws::BM} * gws::BN * sizeof(float);
-// One counter per 32 x 32 chunk of a part: 4 lane quarters x 8 subtiles.
-constexpr size_t kCountersPerPart = 4 * gws::SUB_PER_PART;
-// Workspace bounds (per SM): partial parts and chunk-counter sets.
-constexpr size_t kPartsPerSm = gws::SK_MAX_PIECES_PER_CLUSTER;
-constexpr size_t kCounterSetsPerSm = 2;
+// Workspace: one partial part per CTA of a launch (each runs at most one
+// piece), and per CTA of a split tile 8 epilogue-warp counter pairs.
+constexpr size_t kCounterWordsPerSm = 2 * gws::NUM_EPI_WARPS;
 #ifdef GEMM_WS_DEBUG
 constexpr int kScheduleCols = 15;   // columns of a gemm_ws_debug_schedule row
 #endif
@@ -257,8 +255,8 @@ struct Plan {
   int64_t num_units;   // units (an upper bound of unit ids with stream-K)
   int64_t num_stages;  // ring stages covering K
   int64_t sk_first;    // first tile of the stream-K region (num_tiles: none)
-  int64_t sk_clusters; // clusters sharing the stream-K region
-  int64_t sk_work;     // ring stages in the stream-K region
+  int64_t sk_split;    // pieces per tile of the region
+  int64_t sk_clusters; // clusters running pieces
   int64_t clusters;    // persistent clusters launched
 };
 
@@ -298,8 +296,8 @@ Plan make_plan(const gemm_ws* h, int64_t M, int64_t N, int64_t K, int64_t L, boo
   q.num_units = q.num_full + 2 * (T - q.num_full);
   q.clusters = q.num_units < P ? q.num_units : P;
   q.sk_first = T;
+  q.sk_split = 1;
   q.sk_clusters = 0;
-  q.sk_work = 0;
   // Stream-out keeps whole tiles: its consumer takes every tile where the
   // epilogue computes it.
   if (streamout || h->stream_k == 0 || !h->partial || P < 2) return q;
@@ -311,15 +309,15 @@ Plan make_plan(const gemm_ws* h, int64_t M, int64_t N, int64_t K, int64_t L, boo
   if (S > ns / min_share) S = ns / min_share;
   if (S > (forced ? kMaxSplitForced : kMaxSplit)) S = forced ? kMaxSplitForced : kMaxSplit;
   if (S < 2) return q;
-  const int64_t F = T - R, Pe = R * S, W = R * ns;
+  const int64_t F = T - R, Pe = R * S;
   const double sk_cost = static_cast<double>(F / P) + static_cast<double>((ns + S - 1) / S) / ns +
                          kPieceCostStages / static_cast<double>(ns);
   if (!forced && !(sk_cost < dp_cost - 1e-9)) return q;
   q.sk_first = F;
+  q.sk_split = S;
   q.sk_clusters = Pe;
-  q.sk_work = W;
   q.num_full = T;
-  q.num_units = F + Pe * gws::SK_MAX_PIECES_PER_CLUSTER;
+  q.num_units = F + Pe;
   q.clusters = F > 0 ? P : Pe;
   return q;
 }
@@ -376,8 +374,7 @@ int launch(gemm_ws* h, const uint16_t* A, const uint16_t* B, const uint16_t* C, 
   p.num_kb = static_cast<int>((K + gws::BK - 1) / gws::BK);
   p.num_stages = static_cast<int>(q.num_stages);
   p.sk_first = static_cast<int>(q.sk_first);
-  p.sk_clusters = static_cast<int>(q.sk_clusters);
-  p.sk_work = q.sk_work;
+  p.sk_split = static_cast<int>(q.sk_split);
   p.partial = h->partial;
   p.split_count = h->split_count;
   p.group_m = h->group_m;
@@ -549,11 +546,10 @@ int gemm_ws_create(gemm_ws_t** out, int device) {
   if (e == cudaSuccess && h->multicast == 2 && h->cta_group == 1) h->multicast = 1;
   if (e == cudaSuccess) e = cudaMalloc(&h->work, kWorkWords * sizeof(uint32_t));
   if (e == cudaSuccess) e = cudaMemset(h->work, 0, kWorkWords * sizeof(uint32_t));
-  // Stream-K workspace: each cluster runs at most three pieces (one partial
-  // part per CTA each), and the region holds under two waves of tiles.
-  const size_t counter_bytes = h->num_sms * kCounterSetsPerSm * kCountersPerPart * 4;
+  // Stream-K workspace (see kCounterWordsPerSm).
+  const size_t counter_bytes = h->num_sms * kCounterWordsPerSm * 4;
   if (e == cudaSuccess)
-    e = cudaMalloc(&h->partial, static_cast<size_t>(h->num_sms) * kPartsPerSm * kPartBytes);
+    e = cudaMalloc(&h->partial, static_cast<size_t>(h->num_sms) * kPartBytes);
   if (e == cudaSuccess) e = cudaMalloc(&h->split_count, counter_bytes);
   if (e == cudaSuccess) e = cudaMemset(h->split_count, 0, counter_bytes);
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
@@ -628,8 +624,7 @@ int gemm_ws_query_status(gemm_ws_t* h, void* stream) {
     // counter part-way: start the next launch from zero.
     e = cudaMemset(h->work, 0, kWorkWords * sizeof(uint32_t));
     if (e == cudaSuccess)
-      e = cudaMemset(h->split_count, 0,
-                     static_cast<size_t>(h->num_sms) * kCounterSetsPerSm * kCountersPerPart * 4);
+      e = cudaMemset(h->split_count, 0, static_cast<size_t>(h->num_sms) * kCounterWordsPerSm * 4);
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
     if (e != cudaSuccess) return cuda_fail(h, e);
   }
@@ -712,8 +707,7 @@ int gemm_ws_debug_schedule(int cta_group, int multicast, int num_sms, int max_cl
   p.num_units = static_cast<int>(q.num_units);
   p.num_stages = static_cast<int>(q.num_stages);
   p.sk_first = static_cast<int>(q.sk_first);
-  p.sk_clusters = static_cast<int>(q.sk_clusters);
-  p.sk_work = q.sk_work;
+  p.sk_split = static_cast<int>(q.sk_split);
   p.group_m = h.group_m;
   plan[0] = q.cs;
   plan[1] = static_cast<int>(q.clusters);

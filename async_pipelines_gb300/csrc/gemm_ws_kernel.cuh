@@ -157,13 +157,11 @@ struct Params {
   int num_full;                  // tiles [0, num_full) run whole; the rest as two halves
   int num_units;                 // work units (see unit_coords)
   int num_stages;                // ring stages covering K (KSUB k-blocks each)
-  // Stream-K: tiles [sk_first, num_tiles) pool their ring stages (sk_work in
-  // all) and sk_clusters clusters take equal shares; sk_first == num_tiles:
-  // no stream-K region.
+  // Stream-K: the K ranges of tiles [sk_first, num_tiles) are cut into
+  // sk_split equal pieces; sk_first == num_tiles: none.
   int sk_first;
-  int sk_clusters;
-  long long sk_work;
-  float* partial;                // piece partials: [slot][CTA][chunk] x 1024 fp32
+  int sk_split;
+  float* partial;                // piece partials: [cluster][CTA][chunk] x 1024 fp32
   uint32_t* split_count;         // [stream-K tile][CTA][chunk] pieces written (returned to 0)
   int group_m;                   // raster: tiles walk group_m m-tiles per n step
   int staging_tiles_m;           // ceil(M / 128)
@@ -211,12 +209,9 @@ struct Unit {
   int kb0, kb1;        // ring stages [kb0, kb1) of the tile's K range
   int piece, pieces;   // piece `piece` of the `pieces` that share the K range (1: whole)
   int sk_tile;         // index in the stream-K region (chunk counters)
-  int first_cluster;   // cluster that runs piece 0
+  int first_cluster;   // cluster that runs piece 0 (piece k runs on first_cluster + k)
   int id;              // unit number (trace index)
 };
-
-// Most pieces one cluster's share of the stream-K region can touch.
-constexpr int SK_MAX_PIECES_PER_CLUSTER = 3;
 
 __host__ __device__ __forceinline__ Unit whole_tile(const Params& p, int t) {
   Unit w;
@@ -247,28 +242,20 @@ __host__ __device__ __forceinline__ Unit unit_coords(const Params& p, int u) {
   return w;
 }
 
-// Stream-K region: tile r of it owns ring stages [r*ns, (r+1)*ns) of
-// sk_work = (#tiles) * ns; cluster c (< sk_clusters) owns stages
-// [c*sk_work/sk_clusters, (c+1)*sk_work/sk_clusters), cut at tile edges into
-// pieces (a work unit with its own k-tile start and count, as in the SM90
-// cooperative kernel's operator()). Every piece's place follows from this
-// arithmetic alone, so no role needs to exchange schedule information.
-__host__ __device__ __forceinline__ long long sk_begin(const Params& p, int c) {
-  return static_cast<long long>(c) * p.sk_work / p.sk_clusters;
-}
-// The cluster whose share holds stage s.
-__host__ __device__ __forceinline__ int sk_owner(const Params& p, long long s) {
-  return static_cast<int>(((s + 1) * p.sk_clusters - 1) / p.sk_work);
-}
-// Workspace slot of piece k of stream-K tile r: its cluster's j-th piece.
-__host__ __device__ __forceinline__ int sk_slot(const Params& p, const Unit& w, int k) {
-  const int c = w.first_cluster + k;
-  const int j = w.sk_tile - static_cast<int>(sk_begin(p, c) / p.num_stages);
-  return c * SK_MAX_PIECES_PER_CLUSTER + j;
+// Workspace slot of piece k of a stream-K tile: the cluster that runs it.
+__host__ __device__ __forceinline__ int sk_slot(const Params&, const Unit& w, int k) {
+  return w.first_cluster + k;
 }
 
 // The i-th unit of cluster c (of `clusters`), in the order every role of the
-// cluster walks them; false once the cluster has no more.
+// cluster walks them; false once the cluster has no more. With a stream-K
+// region, every cluster first runs its whole tiles (tile c, c + clusters,
+// ...; sk_first is a multiple of clusters), then cluster c = r * S + s (S =
+// sk_split) runs piece s of the region's tile r as its last unit: ring stages
+// [s * ns / S, (s + 1) * ns / S), a work unit with its own k-tile start and
+// count, as in the SM90 cooperative kernel's operator(). Piece s of every
+// tile covers the same k range. Every unit's place follows from this
+// arithmetic alone, so no role needs to exchange schedule information.
 __host__ __device__ __forceinline__ bool next_unit(const Params& p, int c, int clusters, int i, Unit& w) {
   if (p.sk_first >= p.num_tiles) {   // whole tiles, then halves: static stride
     const int u = c + i * clusters;
@@ -276,26 +263,23 @@ __host__ __device__ __forceinline__ bool next_unit(const Params& p, int c, int c
     w = unit_coords(p, u);
     return true;
   }
-  const int dp = p.sk_first / clusters;   // whole tiles of each cluster (a multiple)
+  const int dp = p.sk_first / clusters;
   if (i < dp) {
     w = whole_tile(p, c + i * clusters);
     return true;
   }
-  if (c >= p.sk_clusters) return false;
-  const int j = i - dp;
+  const int S = p.sk_split;
+  if (i > dp || c >= (p.num_tiles - p.sk_first) * S) return false;
+  const int r = c / S, sp = c - r * S;
   const long long ns = p.num_stages;
-  const long long s0 = sk_begin(p, c), s1 = sk_begin(p, c + 1);
-  const int r = static_cast<int>(s0 / ns) + j;
-  const long long ts = static_cast<long long>(r) * ns;
-  if (ts >= s1) return false;
   w = whole_tile(p, p.sk_first + r);
-  w.kb0 = static_cast<int>((s0 > ts ? s0 : ts) - ts);
-  w.kb1 = static_cast<int>((s1 < ts + ns ? s1 : ts + ns) - ts);
-  w.first_cluster = sk_owner(p, ts);
-  w.pieces = sk_owner(p, ts + ns - 1) - w.first_cluster + 1;
-  w.piece = c - w.first_cluster;
+  w.kb0 = static_cast<int>(sp * ns / S);
+  w.kb1 = static_cast<int>((sp + 1) * ns / S);
+  w.piece = sp;
+  w.pieces = S;
   w.sk_tile = r;
-  w.id = p.sk_first + c * SK_MAX_PIECES_PER_CLUSTER + j;
+  w.first_cluster = r * S;
+  w.id = p.sk_first + c;
   return true;
 }
 

@@ -26,9 +26,8 @@
  * Ownership: every data pointer is a borrowed DEVICE pointer on the handle's
  * device; the caller owns it and keeps it alive until the stream work ends.
  * The handle owns only its device workspace: the stream-out sequence
- * counter, a status word, a completion count, and the split-K area (up to
- * three 128 x 256 fp32 partials and 64 counter words per SM, ~384 KiB per
- * SM).
+ * counter, a status word, a completion count, and the split-K area (one
+ * 128 x 256 fp32 partial and 16 counter words per SM, ~128 KiB per SM).
  * The kernel returns every counter to zero before it ends, so runs need no
  * clearing between them; runs on one handle that overlap on the GPU (e.g. on
  * two streams) race on that workspace: serialise them or use one handle per

@@ -9,7 +9,7 @@ many problem shapes, device shapes and stream-K settings, that
 - the pieces of a stream-K tile are numbered 0..n-1 by consecutive clusters,
   in K order, and all agree on n and on the first cluster;
 - every workspace slot and chunk-counter index stays inside the buffers the
-  handle allocates (3 partial parts and 2 counter sets per SM), slots are
+  handle allocates (one partial part and 16 counter words per SM), slots are
   never shared, and unit ids are unique and below the reported bound;
 - every cluster runs at most one piece, as its last unit, all pieces are
   equal within one stage, and piece s of every tile starts at the same k;
@@ -117,8 +117,8 @@ def check(plan, rows, dev, M, N, K, L):
     assert np.all(R["sk_tile"][split] == R["tile"][split] - sk_first)
     slots = R["slot"][split]
     assert len(set(slots.tolist())) == len(slots)
-    assert slots.min() >= 0 and (slots.max() + 1) * cs <= 3 * sms          # partial parts
-    assert (R["sk_tile"][split].max() + 1) * cs * 32 <= 2 * sms * 32      # chunk counters
+    assert slots.min() >= 0 and (slots.max() + 1) * cs <= sms               # partial parts
+    assert (R["sk_tile"][split].max() + 1) * cs * 16 <= sms * 16          # counter words
     for t in np.unique(R["tile"][split]):
         sel = R["tile"] == t
         n_p = R["pieces"][sel]
