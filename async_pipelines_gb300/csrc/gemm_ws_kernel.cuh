@@ -162,7 +162,8 @@ struct Params {
   int sk_first;
   int sk_split;
   float* partial;                // piece partials: [cluster][CTA][chunk] x 1024 fp32
-  uint32_t* split_count;         // [stream-K tile][CTA][chunk] pieces written (returned to 0)
+  uint32_t* split_count;         // [stream-K tile][CTA][epilogue warp] {pieces counted in,
+                                 // owners done}, returned to 0 by the last owner
   int group_m;                   // raster: tiles walk group_m m-tiles per n step
   int staging_tiles_m;           // ceil(M / 128)
   int staging_tiles_n;           // ceil(N / 128)
@@ -208,7 +209,7 @@ struct Unit {
   int tile;    // tile index
   int kb0, kb1;        // ring stages [kb0, kb1) of the tile's K range
   int piece, pieces;   // piece `piece` of the `pieces` that share the K range (1: whole)
-  int sk_tile;         // index in the stream-K region (chunk counters)
+  int sk_tile;         // index in the stream-K region (fix-up counters)
   int first_cluster;   // cluster that runs piece 0 (piece k runs on first_cluster + k)
   int id;              // unit number (trace index)
 };

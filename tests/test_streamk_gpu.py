@@ -9,7 +9,7 @@ the owner waits for them, adds them to its own accumulator in piece order
 (so the bits do not depend on which piece owns a chunk) and runs the
 alpha/beta epilogue. These tests check that the launch plan really splits,
 compare with the oracle, and check that back-to-back launches and graph
-replays (whose chunk counters the kernel returns to zero) stay correct.
+replays (whose fix-up counters the kernel returns to zero) stay correct.
 GEMM_WS_STREAM_K=2 splits shapes the cost model would run whole, down to
 one-stage pieces, so that many pieces, ragged K and a whole-tile part before
 the split tiles are covered at sizes the oracle checks quickly.
