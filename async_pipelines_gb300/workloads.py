@@ -93,6 +93,22 @@ WORKLOADS = {
 HEADLINE = "gemm_8192x8192x8192_alpha_beta"
 STREAMOUT = "gemm_streamout_8192x8192x4096"
 
+# Informational shapes beside the five above (measured, not parity configs):
+# a skinny GEMM bound by writing D.
+EXTRA_WORKLOADS = {
+    w.name: w
+    for w in [
+        Workload("gemm_8192x8192x64_skinny", 8192, 8192, 64, 1,
+                 ("uniform",), None, 1.0, 0.0, seed=6),
+    ]
+}
+SKINNY = "gemm_8192x8192x64_skinny"
+
+
+def workload(name: str) -> Workload:
+    """A workload of either table by name."""
+    return WORKLOADS[name] if name in WORKLOADS else EXTRA_WORKLOADS[name]
+
 
 def _draw(gen: torch.Generator, shape, dist) -> torch.Tensor:
     if dist[0] == "uniform":

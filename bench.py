@@ -301,8 +301,7 @@ def other_workloads(g, dev, stream, steps: int = 30):
     cases = [(workloads.WORKLOADS["gemm_256x256x256"], "us"),
              (workloads.WORKLOADS["gemm_4096x4096x4096"], "tflops"),
              (workloads.WORKLOADS["gemm_batched4_5000x3000x4000_ragged"], "tflops"),
-             (workloads.Workload("gemm_8192x8192x64_skinny", 8192, 8192, 64, 1, ("uniform",),
-                                 None, 1.0, 0.0, seed=6), "gbs")]
+             (workloads.EXTRA_WORKLOADS[workloads.SKINNY], "gbs")]
     for w, kind in cases:
         A, B, C = workloads.workload_inputs(w)
         Ad, Bd = A.to(dev), B.to(dev)
@@ -473,7 +472,7 @@ def run_kernel_only(args, local):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     g = gemm_ws.GemmWS(local)
-    w = workloads.WORKLOADS[args.workload or workloads.HEADLINE]
+    w = workloads.workload(args.workload or workloads.HEADLINE)
     A, B, C = workloads.workload_inputs(w)
     Ad, Bd = A.to(dev), B.to(dev)
     Cd = C.to(dev) if C is not None else None
@@ -584,7 +583,8 @@ def main():
     ap.add_argument("--overhead-reps", type=int, default=30)
     ap.add_argument("--kernel-only", action="store_true",
                     help="launch only the GEMM of --workload (for profilers); no contract line")
-    ap.add_argument("--workload", choices=sorted(workloads.WORKLOADS), default=None)
+    ap.add_argument("--workload", choices=sorted(workloads.WORKLOADS) + sorted(workloads.EXTRA_WORKLOADS),
+                    default=None)
     ap.add_argument("--vs-library", action="store_true",
                     help="interleaved rounds against torch.addmm (cuBLAS) on the headline "
                          "workload; a cross-check, no contract line")
