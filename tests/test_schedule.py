@@ -28,8 +28,8 @@ from async_pipelines_gb300 import gemm_ws
 BM, BN, BK = 128, 256, 64
 
 # (cta_group, multicast, SMs, clusters that fit): CTA pairs and single CTAs
-# on 152 and 148 SMs, and 4-CTA multicast clusters.
-DEVICES = [(2, 1, 152, 76), (1, 1, 152, 152), (2, 2, 152, 38), (2, 1, 148, 74)]
+# on 152 and 148 SMs, and 4-CTA multicast clusters (36 fit on a 152-SM GB300).
+DEVICES = [(2, 1, 152, 76), (1, 1, 152, 152), (2, 2, 152, 36), (2, 1, 148, 74)]
 DEVICE_IDS = ["pair152", "single152", "quad152", "pair148"]
 
 SHAPES = [
