@@ -314,6 +314,9 @@ def other_workloads(g, dev, stream, steps: int = 30):
         rec = {"ms_per_launch": round(ms, 5)}
         if kind == "us":
             rec["us_per_launch"] = round(ms * 1e3, 2)
+            # The same calls captured once in a CUDA graph and replayed: the
+            # device time per GEMM without the per-call host path.
+            rec["us_per_gemm_graph_replay"] = round(graph_replay_us(g, Ad, Bd, Cd, D, w, dev), 2)
         if kind in ("tflops", "us"):
             rec["tflops"] = round(w.flops / (ms * 1e-3) / 1e12, 2)
         if kind == "gbs":
@@ -323,6 +326,32 @@ def other_workloads(g, dev, stream, steps: int = 30):
         del A, B, C, Ad, Bd, Cd, D
     torch.cuda.empty_cache()
     return out
+
+
+def graph_replay_us(g, Ad, Bd, Cd, D, w, dev, per_graph: int = 20, replays: int = 10) -> float:
+    """Median device time per GEMM over replays of a CUDA graph holding
+    `per_graph` back-to-back calls (CUDA events around each replay)."""
+    s = torch.cuda.Stream(device=dev)
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        for _ in range(3):
+            g.run(Ad, Bd, Cd, D, w.alpha, w.beta, stream=s)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        for _ in range(per_graph):
+            g.run(Ad, Bd, Cd, D, w.alpha, w.beta, stream=s)
+    graph.replay()
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(replays):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        graph.replay()
+        b.record()
+        torch.cuda.synchronize()
+        times.append(a.elapsed_time(b) * 1e3 / per_graph)
+    return statistics.median(times)
 
 
 def run_ours(args, rank, world, local):

@@ -252,6 +252,39 @@ def test_random_shapes_match_oracle(gw_each, case):
     assert_gemm_close(d, ref, K, f"{M}x{N}x{K}x{L}")
 
 
+def _random_auto_cases(n, seed):
+    """Shapes that reach every path the default handle picks per problem:
+    short K (single-CTA tiles), long K on few tiles (split pieces), and the
+    rest (CTA pairs, with half-width tail tiles)."""
+    rng = np.random.default_rng(seed)
+    for i in range(n):
+        kind = i % 3
+        if kind == 0:     # short K
+            M, N, K = int(rng.integers(1, 3000)), 8 * int(rng.integers(1, 400)), 8 * int(rng.integers(1, 64))
+        elif kind == 1:   # few tiles, long K
+            M, N, K = int(rng.integers(1, 900)), 8 * int(rng.integers(1, 110)), 8 * int(rng.integers(512, 2500))
+        else:             # many tiles
+            M, N, K = int(rng.integers(1500, 5000)), 8 * int(rng.integers(190, 600)), 8 * int(rng.integers(130, 400))
+        L = int(rng.integers(1, 3))
+        alpha = float(np.float32(rng.choice([1.0, -0.5, 2.0])))
+        beta = float(np.float32(rng.choice([0.0, 1.0, -1.5])))
+        yield M, N, K, L, alpha, beta
+
+
+@pytest.mark.parametrize("case", list(_random_auto_cases(12, seed=77)),
+                         ids=lambda c: "x".join(str(v) for v in c[:4]))
+def test_random_shapes_default_handle(gw, case):
+    """Seeded random problems on a default handle (tile configuration and
+    split chosen per problem); sampled rows (every tile edge plus random
+    rows) against the oracle."""
+    M, N, K, L, alpha, beta = case
+    cd = ("uniform",) if beta != 0 else None
+    rows = sample_rows(M, L, 16, seed=K + N)
+    d, ref = run_case(gw, M, N, K, L, alpha, beta, ab=("normal", 0.5), cd=cd,
+                      seed=M * 5 + N + K, rows=rows)
+    assert_gemm_close(d, ref, K, f"{M}x{N}x{K}x{L}")
+
+
 def test_d_neighbours_are_never_written(gw_each):
     """D lives inside a larger buffer; the elements before and after it (and
     hence outside the ragged M x N edges of the TMA stores) keep their canary
