@@ -46,9 +46,13 @@
 //            (UMMA commits per CTA group, async producers signalling the even
 //            CTA of the pair).
 //
-// Every role walks the same static persistent tile sequence (cluster c takes
-// tiles c, c + #clusters, ...), so the scheduler needs no communication.
-// Every wait is bounded by a watchdog (global timer): on expiry the kernel
+// Every role walks the same static persistent unit sequence (next_unit:
+// cluster c takes tiles c, c + #clusters, ..., and, where the host planned
+// it, one equal piece of a tile's K range as its last unit), so the
+// scheduler needs no communication. The pieces of a tile combine their fp32
+// partials through a workspace in the epilogue (the fix-up step of the SM90
+// cooperative kernel). Every wait is bounded by a watchdog (global timer): on
+// expiry the kernel
 // records GEMM_WS_ERR_TIMEOUT in a status word, all roles leave their loops,
 // in-flight copies are drained and TMEM is freed.
 #pragma once
@@ -663,9 +667,6 @@ __device__ __forceinline__ void epilogue_role(const Params& p, uint32_t sbase, u
           mbar_arrive_cluster(mapa_shared(bar(BAR_ACC_EMPTY + b), rank - rank % CG));
       }
     };
-    // alpha * acc (+ beta * C), rounded to bf16, through a shared-memory slot
-    // to the TMA store of D (and, with stream-out, to the consumer warp).
-    // Returns false if a bounded wait gave up.
     // alpha * acc (+ beta * C) of subtile j, rounded to bf16, through a
     // shared-memory slot to the TMA store of D (and, with stream-out, to the
     // consumer warp). next_c: the subtile whose C load may now reuse this
