@@ -33,6 +33,12 @@
  * two streams) race on that workspace: serialise them or use one handle per
  * stream.
  *
+ * Threads: a handle is not thread-safe (each call also updates its host-side
+ * cache of TMA descriptors); calls on one handle from several host threads
+ * must be serialised by the caller. Different handles are independent.
+ * gemm_ws_run_streamout_noalloc takes a library-wide lock only for its
+ * one-time per-device set-up.
+ *
  * Errors: every entry point returns a gemm_ws_status. A call that returns an
  * error other than GEMM_WS_ERR_CUDA launched nothing and wrote nothing. All
  * runs are asynchronous on `stream` (a cudaStream_t passed as void*, NULL
