@@ -677,7 +677,7 @@ int gemm_ws_debug_schedule(int cta_group, int multicast, int num_sms, int max_cl
                            int stream_k, int64_t M, int64_t N, int64_t K, int64_t L,
                            int streamout, int* rows, int64_t max_rows, int64_t* num_rows,
                            int* plan) {
-  if ((cta_group != 1 && cta_group != 2) || (multicast != 1 && multicast != 2) ||
+  if (cta_group < 0 || cta_group > 2 || (multicast != 1 && multicast != 2) ||
       num_sms < 1 || max_clusters < 1 || !num_rows || !plan || M <= 0 || N <= 0 || K < 0 ||
       L <= 0 || stream_k < 0 || stream_k > 2)
     return GEMM_WS_ERR_INVALID_ARG;

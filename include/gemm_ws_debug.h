@@ -64,7 +64,9 @@ int gemm_ws_debug_launch_shape(gemm_ws_t* h, int64_t M, int64_t N, int64_t K, in
 /* The whole persistent schedule of a launch, on the host, without a handle
  * or a GPU: the plan the library makes for a device with `num_sms` SMs on
  * which `max_clusters` clusters of the chosen shape fit (cta_group 1 or 2,
- * multicast 1 or 2, stream_k 0 off / 1 cost model / 2 always), and the units
+ * or 0 to let the library choose per problem with `max_clusters` CTA pairs
+ * and `num_sms` single CTAs; multicast 1 or 2; stream_k 0 off / 1 cost
+ * model / 2 always), and the units
  * every cluster walks, produced by the kernel's own unit iterator.
  *  - plan[9] = {CTAs per cluster, clusters, unit-id bound, tiles, ring
  *    stages per tile, first stream-K tile, stream-K clusters, tiles_m,

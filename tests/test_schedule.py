@@ -180,3 +180,19 @@ def test_stream_k_where_expected(lib):
     # 152 tiles = exactly two waves of 76 clusters: nothing to balance
     plan, _ = schedule(lib, dev, 2, 76 * 256 * 2, 256, 4096, 1)
     assert plan[3] == 152 and plan[5] == 152
+
+
+@pytest.mark.parametrize("M,N,K,L,cs", [
+    (8192, 8192, 64, 1, 1), (256, 256, 256, 1, 1), (8192, 8192, 512, 1, 1),
+    (2048, 2048, 1024, 1, 1), (3072, 3072, 1024, 1, 1),   # <= 2 waves (144 pair tiles)
+    (3328, 3328, 1024, 1, 2), (8192, 8192, 1024, 1, 2),   # more (169): CTA pairs
+    (512, 512, 2048, 1, 2), (4096, 4096, 4096, 1, 2), (8192, 8192, 8192, 1, 2),
+])
+def test_tile_configuration_rule(lib, M, N, K, L, cs):
+    """Default handles: single-CTA tiles for K <= 512, or K <= 1024 with at
+    most two waves (2 x 76) of 256 x 256 pair tiles; CTA pairs otherwise. The
+    chosen plan still covers every stage exactly once."""
+    dev = (0, 1, 152, 76)
+    plan, rows = schedule(lib, dev, 1, M, N, K, L)
+    assert plan[0] == cs
+    check(plan, rows, (cs, 1, 152, 76 if cs == 2 else 152), M, N, K, L)
