@@ -91,6 +91,7 @@ constexpr uint32_t TMEM_COLS = ACC_BUFS * BN;   // 512: all of the SM's TMEM
 constexpr uint32_t A_SLAB_BYTES = BM * BK * 2;           // 16 KiB: 128 x 64 slab of A
 constexpr uint32_t EPI_QUARTER_BYTES = 32 * EPI_N * 2;   // 2 KiB: one warp's rows
 constexpr uint32_t EPI_SLOT_BYTES = BM * EPI_N * 2;      // 8 KiB: 128 rows
+constexpr uint32_t WIDE_QUARTER_BYTES = 32 * 2 * EPI_N * 2;   // 4 KiB: 32 x 64 block of D
 constexpr uint32_t STATUS_TIMEOUT = 5;   // == GEMM_WS_ERR_TIMEOUT
 constexpr uint32_t WAIT_HINT_NS = 1000000;   // suspend bound of one try_wait
 
@@ -155,6 +156,7 @@ struct Params {
   CUtensorMap tmB2;  // {K, N, L}, box {64, 128 / CG}: B of a half-width unit
   CUtensorMap tmC;   // {N, M, L}, box {32, 32},  64-byte swizzle (beta != 0)
   CUtensorMap tmD;   // {N, M, L}, box {32, 32},  64-byte swizzle
+  CUtensorMap tmDw;  // {N, M, L}, box {64, 32}, 128-byte swizzle (wide stores)
   CUtensorMap tmS;   // staging {128, 128, T}, box {32, 128}, 64-byte swizzle
   int M, N, K, L;
   int tiles_m, tiles_n, num_tiles, num_kb;   // tiles of 128*CG x 256
@@ -173,6 +175,8 @@ struct Params {
   int staging_tiles_n;           // ceil(N / 128)
   float alpha, beta;
   int has_c;                     // beta != 0
+  int wide_d;                    // D stores in 32 x 64 blocks (beta == 0, no stream-out,
+                                 // no split pieces, short K)
   int streamout;
   uint32_t* flags;               // 2 * T words (stream-out)
   uint32_t* counter;             // stream-out sequence counter (zero at launch; the
@@ -630,6 +634,7 @@ __device__ __forceinline__ void epilogue_role(const Params& p, uint32_t sbase, u
   // read, its buffers take the space) or two.
   const uint32_t per_half = (p.has_c ? EPI_SLOTS : EPI_SLOTS_NOC) / 2;
   const uint32_t cbuf = sbase + C::OFF_C + static_cast<uint32_t>(e) * EPI_QUARTER_BYTES;
+  const bool wide = p.wide_d != 0;
   const uint32_t cbar = bar(BAR_C_FULL + e);
   uint32_t u = 0;        // subtiles stored by this warp (slot ring position)
   uint32_t cu = 0;       // C subtiles consumed by this warp
@@ -733,7 +738,51 @@ __device__ __forceinline__ void epilogue_role(const Params& p, uint32_t sbase, u
     const uint32_t tacc = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + b * BN;
 
     bool ok = true;
-    if (!split) {
+    if (wide) {
+      // Short K, without C, stream-out or split pieces in the launch: D goes
+      // out in 32 x 64 blocks (128-byte rows, 128-byte swizzle), half the
+      // TMA store rows of 32 x 32 blocks, which is what bounds a short-K
+      // GEMM's epilogue. Warp (q, hf) takes the unit's 64-column blocks jw
+      // with jw % 2 == hf through its own 4 KiB area of the epilogue region
+      // (laid out differently from the D slots, so a launch never mixes the
+      // two). One block in flight per warp: with longer K, where the
+      // epilogue hides under the MMA, the narrow path's two are better.
+      if (nsub == 0) release_acc();
+      const int nwide = nsub / 2;
+      uint8_t* dq = smem + C::OFF_D + hf * (4 * WIDE_QUARTER_BYTES) + q * WIDE_QUARTER_BYTES;
+      const uint32_t wrow = lane * 128, wswz = lane & 7;
+      for (int jw = hf; jw < nwide; jw += 2) {
+        uint32_t a0[32], a1[32];
+        if (has_acc) {
+          tmem_ld_32x32b_x32(tacc + (2 * jw) * EPI_N, a0);
+          tmem_ld_32x32b_x32(tacc + (2 * jw + 1) * EPI_N, a1);
+          tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int x = 0; x < 32; ++x) a0[x] = a1[x] = 0u;
+        }
+        if (jw + 2 >= nwide) release_acc();
+        if (lane == 0) bulk_wait_read<0>();   // this warp's previous block has been read
+        __syncwarp();
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const uint32_t* a = c < 4 ? a0 : a1;
+          const int o = 8 * (c & 3);
+          uint4 wv;
+          wv.x = pack_bf16x2(p.alpha * __uint_as_float(a[o + 0]), p.alpha * __uint_as_float(a[o + 1]));
+          wv.y = pack_bf16x2(p.alpha * __uint_as_float(a[o + 2]), p.alpha * __uint_as_float(a[o + 3]));
+          wv.z = pack_bf16x2(p.alpha * __uint_as_float(a[o + 4]), p.alpha * __uint_as_float(a[o + 5]));
+          wv.w = pack_bf16x2(p.alpha * __uint_as_float(a[o + 6]), p.alpha * __uint_as_float(a[o + 7]));
+          *reinterpret_cast<uint4*>(dq + wrow + ((c ^ wswz) << 4)) = wv;
+        }
+        fence_proxy_async_smem();   // generic writes -> visible to the TMA (async proxy)
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_3d(&p.tmDw, smem_addr(dq), n0 + jw * 2 * EPI_N, m0, l);
+          bulk_commit();
+        }
+      }
+    } else if (!split) {
       if (nsub == 0) release_acc();   // this CTA's rows lie outside M x N
       for (int j = hf; j < nsub; j += 2) {
         uint32_t acc[32];
@@ -1037,6 +1086,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_ws_kernel(const __grid_co
     }
     if (p.has_c) prefetch_tensormap(&p.tmC);
     prefetch_tensormap(&p.tmD);
+    if (p.wide_d) prefetch_tensormap(&p.tmDw);
     if (p.streamout) prefetch_tensormap(&p.tmS);
   }
   if (warp == WARP_MMA) {

@@ -103,6 +103,24 @@ def test_integer_inputs_bit_exact(gw_each, M, N, K, L):
     np.testing.assert_array_equal(bits_of(D).reshape(L, M, N), f64_to_bf16_bits(ref))
 
 
+@pytest.mark.parametrize("M,N,K,L", [
+    (300, 520, 200, 2),     # ragged M and N (N not a multiple of 64), batches
+    (4000, 4104, 96, 2),    # half-width tail units, ragged N edge inside a 64-column block
+    (130, 8, 64, 1),        # N narrower than one 64-column block
+    (8192, 1024, 64, 1),    # skinny: many units per cluster, blocks in flight back to back
+])
+def test_wide_d_stores_bit_exact(gw_each, M, N, K, L):
+    """beta == 0 and K <= 512: D leaves in 32 x 64 blocks (128-byte swizzle).
+    Integer inputs make the result exact, so it must match bit for bit,
+    including the columns and rows the TMA store clips at ragged edges."""
+    A, B, _ = workloads.make_inputs(M, N, K, L, ("int", -4, 4), None, seed=N + K)
+    D = torch.full((L, M, N), 5.0, dtype=torch.bfloat16, device="cuda")
+    gw_each.run(to_dev(A), to_dev(B), None, D, 0.5, 0.0)
+    torch.cuda.synchronize()
+    ref = oracle.gemm(bits_of(A), bits_of(B), None, M, N, K, L, 0.5, 0.0)
+    np.testing.assert_array_equal(bits_of(D).reshape(L, M, N), f64_to_bf16_bits(ref))
+
+
 # ------------------------------------------------------------------ small shapes
 
 @pytest.mark.parametrize("M,N,K,L,alpha,beta", [
