@@ -1,7 +1,9 @@
 // Host side of the C ABI declared in include/gemm_ws.h: argument checks (the
 // `can_implement` role of "sm90_gemm_tma_warpspecialized_cooperative.hpp"),
-// TMA descriptor encoding, the tiny device workspace, and the launch of the
-// persistent kernel (grid = min(#SMs, #tiles), one CTA per SM).
+// TMA descriptor encoding (cached per handle), the device workspace (counters,
+// status word, stream-K partials), the per-problem plan (tile configuration,
+// half-width tail units or stream-K pieces, persistent grid of at most the
+// co-resident clusters) and the launch, one CTA per SM.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
@@ -22,7 +24,7 @@ struct MapCacheEntry {
   const void* ptr;
   uint64_t d0, d1, d2;
   uint32_t b0, b1;
-  int swizzle;
+  int swizzle, promotion;
   bool valid;
   CUtensorMap map;
 };
@@ -81,7 +83,8 @@ CUresult encode3d(gemm_ws* h, CUtensorMap* m, const void* ptr, uint64_t d0, uint
   for (int i = 0; i < kMapCache; ++i) {
     const MapCacheEntry& e = h->map_cache[i];
     if (e.valid && e.ptr == ptr && e.d0 == d0 && e.d1 == d1 && e.d2 == d2 && e.b0 == b0 &&
-        e.b1 == b1 && e.swizzle == static_cast<int>(sw)) {
+        e.b1 == b1 && e.swizzle == static_cast<int>(sw) &&
+        e.promotion == static_cast<int>(promo)) {
       std::memcpy(m, &e.map, sizeof(CUtensorMap));
       return CUDA_SUCCESS;
     }
@@ -103,6 +106,7 @@ CUresult encode3d(gemm_ws* h, CUtensorMap* m, const void* ptr, uint64_t d0, uint
     e.b0 = b0;
     e.b1 = b1;
     e.swizzle = static_cast<int>(sw);
+    e.promotion = static_cast<int>(promo);
     e.map = *m;
     e.valid = true;
   }
@@ -136,8 +140,8 @@ int check_problem(gemm_ws* h, const uint16_t* A, const uint16_t* B, const uint16
 // units so that the persistent schedule's final wave is not half idle.
 // Cluster c runs units c, c + P, ...; a whole tile costs 1, a half ~0.8
 // (same k-loop and A traffic, half the MMA work: load-bound; 0.79 measured on
-// GB300 at 4096^3). Returns the number of whole
-// tiles (and, in *cost, the slowest cluster's work in tile units); only
+// GB300 at 4096^3). Returns the number of whole tiles (and, in *cost, the
+// slowest cluster's work in tile units); only
 // splits of at most one wave of tiles are considered (with fewer tiles than
 // clusters, splitting spreads a small problem over more SMs).
 int64_t choose_num_full(int64_t tiles, int64_t P, double* cost) {
@@ -203,6 +207,9 @@ cudaError_t configure_kernels(int num_sms, int* max_pair_clusters, int* max_quad
   return e;
 }
 
+// Wide (32 x 64) D stores for K up to this (see launch).
+constexpr int64_t kWideDMaxK = 512;
+
 // Persistent clusters the launch may use: SMs for single CTAs, else the
 // co-resident clusters of the kernel's cluster size.
 int64_t cluster_capacity(const gemm_ws* h, int cs) {
@@ -230,8 +237,6 @@ int64_t cluster_capacity(const gemm_ws* h, int cs) {
 // beats whole tiles with half-width tails; GEMM_WS_STREAM_K=2 takes it
 // wherever the shape allows, with pieces down to one ring stage (tests).
 constexpr int64_t kMinShareK = 1024;
-// Wide (32 x 64) D stores for K up to this.
-constexpr int64_t kWideDMaxK = 512;
 constexpr int64_t kMaxSplit = 16;
 constexpr int64_t kMaxSplitForced = 32;   // owner masks in the kernel hold 32 pieces
 // Fix-up of a split tile, measured on GB300 (accumulator complete -> last D
