@@ -171,6 +171,7 @@ struct Params {
   uint32_t* split_count;         // [stream-K tile][CTA][epilogue warp] {pieces counted in,
                                  // owners done}, returned to 0 by the last owner
   int group_m;                   // raster: tiles walk group_m m-tiles per n step
+  int k_snake;                   // 1: every other unit of a cluster walks K backwards
   int staging_tiles_m;           // ceil(M / 128)
   int staging_tiles_n;           // ceil(N / 128)
   float alpha, beta;
@@ -220,6 +221,7 @@ struct Unit {
   int sk_tile;         // index in the stream-K region (fix-up counters)
   int first_cluster;   // cluster that runs piece 0 (piece k runs on first_cluster + k)
   int id;              // unit number (trace index)
+  int rev;             // the producer walks the k range from its end
 };
 
 __host__ __device__ __forceinline__ Unit whole_tile(const Params& p, int t) {
@@ -236,6 +238,7 @@ __host__ __device__ __forceinline__ Unit whole_tile(const Params& p, int t) {
   w.sk_tile = -1;
   w.first_cluster = 0;
   w.id = t;
+  w.rev = 0;
   return w;
 }
 
@@ -270,11 +273,13 @@ __host__ __device__ __forceinline__ bool next_unit(const Params& p, int c, int c
     const int u = c + i * clusters;
     if (u >= p.num_units) return false;
     w = unit_coords(p, u);
+    w.rev = p.k_snake & i;
     return true;
   }
   const int dp = p.sk_first / clusters;
   if (i < dp) {
     w = whole_tile(p, c + i * clusters);
+    w.rev = p.k_snake & i;
     return true;
   }
   const int S = p.sk_split;
@@ -474,7 +479,10 @@ __device__ __forceinline__ void producer_role(const Params& p, uint32_t sbase, u
     const bool whole = w.width == BN;
     const CUtensorMap* tmb = whole ? &p.tmB : &p.tmB2;
     const uint32_t tx = whole ? C::STAGE_TX : C::STAGE_TX_HALF;
-    for (int kb = w.kb0; kb < w.kb1; ++kb) {
+    for (int it = 0; it < w.kb1 - w.kb0; ++it) {
+      // With k_snake, odd units walk K from the end, so a wave starts on the
+      // k-slices the previous wave loaded last, while L2 still holds them.
+      const int kb = w.rev ? w.kb1 - 1 - it : w.kb0 + it;
       const uint32_t s = g % C::STAGES;
       const uint32_t ph = (g / C::STAGES) & 1;
       if (!token && !wait_spin<MC == 2>(empty(s), ph ^ 1, wd)) {
@@ -554,7 +562,7 @@ __device__ __forceinline__ void mma_role(const Params& p, uint32_t sbase, uint32
     tc_fence_after_sync();   // epilogue's TMEM reads of buffer b precede these MMAs
     {
       const uint32_t d_tmem = tmem_base + b * BN;
-      for (int kb = w.kb0; kb < w.kb1; ++kb) {
+      for (int it = 0; it < w.kb1 - w.kb0; ++it) {   // stages in the order the producer loads them
         const uint32_t s = g % C::STAGES;
         // The stage's bytes are ordered before the MMA by the barrier's
         // transaction count (TMA and tcgen05 both act in the async proxy).
@@ -568,7 +576,7 @@ __device__ __forceinline__ void mma_role(const Params& p, uint32_t sbase, uint32
               sdesc_kmajor_sw128(a_addr + blk * C::A_BLOCK_BYTES + kin * UMMA_K * 2);
           const uint64_t bd =
               sdesc_kmajor_sw128(b_addr + blk * C::B_BLOCK_BYTES + kin * UMMA_K * 2);
-          const uint32_t acc = (kb != w.kb0 || kk != 0) ? 1u : 0u;
+          const uint32_t acc = (it != 0 || kk != 0) ? 1u : 0u;
           if constexpr (CG == 1)
             umma_bf16(d_tmem, ad, bd, idesc, acc);
           else
