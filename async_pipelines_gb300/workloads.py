@@ -13,7 +13,7 @@ with bf16 operands, named by what it is and its sizes:
   cooperative kernel page and of the SM100 mainloop on the discussion page).
 * C and D are row-major ``L x M x N``; batches are packed.
 
-Distributions (readings of the pages' silence, stated once here):
+Distributions (readings where the cited sources are silent, stated once here):
 
 * ``uniform``: fp32 ``torch.rand * 2 - 1`` (so ``[-1, 1)``), rounded to bf16
   round-to-nearest-even.

@@ -96,7 +96,12 @@ int gemm_ws_destroy(gemm_ws_t* h);
  * of the launch resident at once, as on a whole, unshared GPU.
  * GEMM_WS_STREAM_K in the environment at gemm_ws_create sets this per
  * handle: 0 off, 1 (default) by the cost model, 2 wherever the shape allows
- * (pieces down to one ring stage). gemm_ws_run_streamout never splits. */
+ * (pieces down to one ring stage). gemm_ws_run_streamout never splits.
+ * Other per-problem choices change only the fp32 summation order, which is
+ * fixed for a given problem and handle (the same bits on every run): the
+ * tile configuration (CTA pairs or single CTAs; GEMM_WS_CTA_GROUP=1|2 forces
+ * one) and walking every other unit's K range backwards (GEMM_WS_K_SNAKE=0
+ * turns that off). */
 int gemm_ws_run(gemm_ws_t* h, const uint16_t* A, const uint16_t* B,
                 const uint16_t* C, uint16_t* D, int64_t M, int64_t N, int64_t K,
                 int64_t L, float alpha, float beta, void* stream);
@@ -141,7 +146,8 @@ int64_t gemm_ws_streamout_tiles(int64_t M, int64_t N, int64_t L);
 
 /* gemm_ws_run_streamout for callers that cannot allocate device memory.
  *
- * No counterpart on the pages: this is a library convenience. Some callers
+ * The cited CUTLASS sources have no counterpart: this is a library
+ * convenience. Some callers
  * may not call cudaMalloc (code that runs inside another allocator's hook, a
  * framework that owns and pools every device allocation, a process that
  * reserved all device memory up front), so they cannot create the handle,

@@ -4,8 +4,8 @@
 // benchmark's CPU-baseline leg may load this library. The product path never
 // calls it; it shares no source, header or helper with the CUDA library.
 //
-// What it computes is the plain definition of the GEMM that the pages'
-// kernels implement: the epilogue of "sm90_gemm_tma_warpspecialized_cooperative.hpp"
+// What it computes is the plain definition of the GEMM that the cited
+// CUTLASS kernels implement: the epilogue of "sm90_gemm_tma_warpspecialized_cooperative.hpp"
 // (the C-load collective and `collective_epilogue.store`) forms
 // alpha * accumulator + beta * C per output element, where the accumulator is
 // the sum over k of A(m,k) * B(k,n) for one (m, n, l) of the MNKL problem
@@ -18,7 +18,7 @@
 // per batch, stored as L x N x K with K contiguous; C is L x M x N row-major.
 // Inputs are raw bf16 bit patterns; the result is left in fp64 (not rounded).
 //
-// Readings where the pages are silent: with beta == 0 the C term is skipped,
+// Readings where those sources are silent: with beta == 0 the C term is skipped,
 // not multiplied by zero (so C may be absent); alpha and beta are fp32 values
 // widened to fp64.
 #include <cstdint>
