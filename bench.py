@@ -609,7 +609,8 @@ def main():
                     help="seconds of CPU oracle work: the baseline sample, or the whole "
                          "reference arm")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--overhead-reps", type=int, default=30)
+    ap.add_argument("--overhead-reps", type=int, default=100,
+                    help="interleaved plain / stream-out launch pairs for the overhead median")
     ap.add_argument("--kernel-only", action="store_true",
                     help="launch only the GEMM of --workload (for profilers); no contract line")
     ap.add_argument("--workload", choices=sorted(workloads.WORKLOADS) + sorted(workloads.EXTRA_WORKLOADS),
