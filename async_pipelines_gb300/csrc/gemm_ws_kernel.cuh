@@ -860,7 +860,13 @@ __device__ __forceinline__ void epilogue_role(const Params& p, uint32_t sbase, u
       if (valid > 0) {
         fence_acq_rel_gpu();   // this lane's partials before the count (the warp syncs below)
         __syncwarp();
+#ifdef GEMM_WS_DEBUG
+        // injected fault 2: piece 1 never counts in, so owners can only stop
+        // waiting through the watchdog
+        if (lane == 0 && !(p.debug_fault == 2 && w.piece == 1)) red_release_gpu_add(cnt, 1u);
+#else
         if (lane == 0) red_release_gpu_add(cnt, 1u);
+#endif
       }
 #ifdef GEMM_WS_DEBUG
       if (p.phases && e == 0 && lane == 0) p.phases[blockIdx.x * 8 + 4] = global_timer_ns();
