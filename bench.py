@@ -225,6 +225,24 @@ def time_launches(fn, steps: int, stream) -> float:
     return start.elapsed_time(end) / steps
 
 
+def time_scrubbed(fn, runs: int, stream, scrub) -> float:
+    """Median ms of single calls of `fn`, each one after a write of `scrub`
+    (256 MiB, twice the L2), so that no call finds its inputs in L2. CUDA
+    events on `stream` bracket the call alone, not the scrub."""
+    pairs = []
+    for i in range(runs):
+        scrub.fill_(i & 0xFF)
+        start = torch.cuda.Event(enable_timing=True)
+        end = torch.cuda.Event(enable_timing=True)
+        start.record(stream)
+        fn()
+        end.record(stream)
+        pairs.append((start, end))
+    torch.cuda.synchronize()
+    ms = sorted(s.elapsed_time(e) for s, e in pairs)
+    return ms[len(ms) // 2]
+
+
 def time_e2e_serial(g, w, Ah, Bh, Ch, Ad, Bd, Cd, D, stream, warmup, steps, world):
     """ms per step of copy-in, GEMM, copy-out, one after another on one stream."""
     Dh = torch.empty(D.shape, dtype=D.dtype).pin_memory()
@@ -298,6 +316,10 @@ def other_workloads(g, dev, stream, steps: int = 30):
     of the 256^3 GEMM (latency-bound), and the HBM bandwidth of a skinny
     8192 x 8192 x 64 GEMM (bound by writing D)."""
     out = {}
+    # Both of these fit in L2 (96 MiB of operands at 4096^3), so they are
+    # also timed with the L2 scrubbed before every call.
+    scrubbed = ("gemm_256x256x256", "gemm_4096x4096x4096")
+    scrub = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     cases = [(workloads.WORKLOADS["gemm_256x256x256"], "us"),
              (workloads.WORKLOADS["gemm_4096x4096x4096"], "tflops"),
              (workloads.WORKLOADS["gemm_batched4_5000x3000x4000_ragged"], "tflops"),
@@ -319,11 +341,17 @@ def other_workloads(g, dev, stream, steps: int = 30):
             rec["us_per_gemm_graph_replay"] = round(graph_replay_us(g, Ad, Bd, Cd, D, w, dev), 2)
         if kind in ("tflops", "us"):
             rec["tflops"] = round(w.flops / (ms * 1e-3) / 1e12, 2)
+        if w.name in scrubbed:
+            cold = time_scrubbed(step, 20, stream, scrub)
+            rec["l2_scrubbed"] = {"ms_median_of_20": round(cold, 5),
+                                  "us": round(cold * 1e3, 2),
+                                  "tflops": round(w.flops / (cold * 1e-3) / 1e12, 2)}
         if kind == "gbs":
             rec["gbs"] = round(w.algorithmic_bytes() / (ms * 1e-3) / 1e9, 1)
             rec["algorithmic_bytes"] = w.algorithmic_bytes()
         out[w.name] = rec
         del A, B, C, Ad, Bd, Cd, D
+    del scrub
     torch.cuda.empty_cache()
     return out
 
