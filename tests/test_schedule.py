@@ -196,3 +196,24 @@ def test_tile_configuration_rule(lib, M, N, K, L, cs):
     plan, rows = schedule(lib, dev, 1, M, N, K, L)
     assert plan[0] == cs
     check(plan, rows, (cs, 1, 152, 76 if cs == 2 else 152), M, N, K, L)
+
+
+@pytest.mark.parametrize("stream_k", [1, 2], ids=["sk_auto", "sk_always"])
+def test_schedule_random_shapes(lib, stream_k):
+    """Seeded random shapes (ragged M, N multiples of 8, K multiples of 8 up
+    to 40k, L up to 4) on every device shape, including the default tile
+    rule: every plan still covers every stage exactly once and keeps its
+    pieces and workspace indices in bounds."""
+    rng = np.random.default_rng(20261202 + stream_k)
+    devices = DEVICES + [(0, 1, 152, 76)]
+    for _ in range(60):
+        M = int(rng.integers(1, 12000))
+        N = 8 * int(rng.integers(1, 1500))
+        K = 8 * int(rng.integers(0, 5000))
+        L = int(rng.integers(1, 5))
+        for dev in devices:
+            plan, rows = schedule(lib, dev, stream_k, M, N, K, L)
+            cs = plan[0]
+            # the default rule picks per problem; check against the config it chose
+            eff = dev if dev[0] else (cs, 1, 152, 76 if cs == 2 else 152)
+            check(plan, rows, eff, M, N, K, L)
