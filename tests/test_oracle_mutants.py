@@ -21,6 +21,11 @@ MUTANTS = [
     ("fp32_accumulator", "double s = 0.0;", "float s = 0.0f;"),
     ("c_transposed", "p.C[(l * p.M + i) * p.N + j]", "p.C[(l * p.N + j) * p.M + i]"),
     ("b_batch_ignored", "p.B[(l * p.N + j) * p.K + k]", "p.B[(j) * p.K + k]"),
+    ("bf16_decode_shift", "bits) << 16", "bits) << 15"),
+    ("alpha_dropped", "double v = p.alpha * s;", "double v = s;"),
+    ("k_starts_at_one", "int64_t k = 0; k < p.K", "int64_t k = 1; k < p.K"),
+    ("batch_row_split", "const int64_t l = g / p.M;\n  const int64_t i = g % p.M;",
+     "const int64_t l = g % p.L;\n  const int64_t i = g / p.L;"),
 ]
 
 PINS = [
