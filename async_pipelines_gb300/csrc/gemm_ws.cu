@@ -650,10 +650,13 @@ int gemm_ws_query_status(gemm_ws_t* h, void* stream) {
   if (e != cudaSuccess) return cuda_fail(h, e);
   if (st != 0) {
     // An aborted launch may leave split-K counters and the stream-out
-    // counter part-way: start the next launch from zero.
-    e = cudaMemset(h->work, 0, kWorkWords * sizeof(uint32_t));
+    // counter part-way: start the next launch from zero. The clears go on
+    // `s` and are waited for, so they are complete before this returns
+    // whatever stream the next run uses.
+    e = cudaMemsetAsync(h->work, 0, kWorkWords * sizeof(uint32_t), s);
     if (e == cudaSuccess)
-      e = cudaMemset(h->split_count, 0, static_cast<size_t>(h->num_sms) * kCounterWordsPerSm * 4);
+      e = cudaMemsetAsync(h->split_count, 0,
+                          static_cast<size_t>(h->num_sms) * kCounterWordsPerSm * 4, s);
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
     if (e != cudaSuccess) return cuda_fail(h, e);
   }
@@ -900,6 +903,7 @@ extern "C" int gemm_ws_run_streamout_noalloc(const uint16_t* A, const uint16_t* 
   h.pdl = pdl_from_env();
   h.max_quad_clusters = d->max_quad_clusters;
   h.group_m = group_m_from_env();
+  h.k_snake = k_snake_from_env();   // same schedule, hence same bits, as a handle
   h.max_pair_clusters = d->max_pair_clusters;
   h.work = d->scratch;
   h.timeout_ns = d->timeout_ns;

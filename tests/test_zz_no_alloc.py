@@ -8,6 +8,7 @@ passes alone in a fresh process as well.
 """
 from __future__ import annotations
 
+import numpy as np
 import pytest
 import torch
 
@@ -43,6 +44,8 @@ def test_noalloc_matches_handle_entry_point_twice_in_a_row():
         assert rc == gemm_ws.OK, gemm_ws.status_string(rc)
         torch.cuda.synchronize()
         assert_gemm_close(bits_of(D), ref, K, f"no-alloc call {call}")
+        # same tile configuration and schedule as the handle: the same bits
+        assert np.array_equal(bits_of(D), bits_of(D_ref)), f"no-alloc call {call}"
         check_staging(D, staging, flags)
 
 
