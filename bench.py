@@ -410,6 +410,13 @@ def run_ours(args, rank, world, local):
         raise RuntimeError(f"device status after timing: {gemm_ws.status_string(status)}")
     tflops_rank = w.flops / (ms * 1e-3) / 1e12
     value = job_throughput(w.flops, world, ms)
+    # Informational: 20 single launches, each timed alone (events around one
+    # call, synchronised between calls), median and best.
+    singles = sorted(time_launches(step, 1, stream) for _ in range(20))
+    single = {"n": len(singles), "median_ms": round(statistics.median(singles), 4),
+              "best_ms": round(singles[0], 4),
+              "median_tflops": round(w.flops / (statistics.median(singles) * 1e-3) / 1e12, 2),
+              "best_tflops": round(w.flops / (singles[0] * 1e-3) / 1e12, 2)}
 
     # End to end through the C ABI with host buffers: every step copies its
     # inputs A, B, C in from pinned host memory and reads D back. The timed
@@ -494,6 +501,7 @@ def run_ours(args, rank, world, local):
                    "l2": "inputs larger than L2 (512 MiB per step), no flush"},
         "pct_of_nominal_2250_tflops": round(100.0 * tflops_rank / NOMINAL_BF16_TFLOPS, 2),
         "pct_of_measured_bf16_burst": round(100.0 * tflops_rank / peak, 2),
+        "single_launch": single,
         "streamout_overhead_pct": round(overhead, 2),
         "streamout": {"workload": so.name, "plain_ms_median": round(mp, 4),
                       "streamout_ms_median": round(ms_so, 4), "reps": len(t_plain),
