@@ -217,3 +217,35 @@ def test_schedule_random_shapes(lib, stream_k):
             # the default rule picks per problem; check against the config it chose
             eff = dev if dev[0] else (cs, 1, 152, 76 if cs == 2 else 152)
             check(plan, rows, eff, M, N, K, L)
+
+
+def _model_best_halves(T, P, half_cost=0.8):
+    """The tail rule stated for the schedule, by exhaustive search: split the
+    last s tiles (s <= min(P, T)) into two half units each, so as to minimise
+    the slowest cluster's work (whole unit 1, half unit half_cost); ties keep
+    fewer halves."""
+    best = None
+    for s in range(0, min(P, T) + 1):
+        F, U = T - s, T + s
+        n_full, n_units = -(-F // P), -(-U // P)
+        worst = n_full + half_cost * (n_units - n_full)
+        if best is None or worst < best[0] - 1e-9:
+            best = (worst, s)
+    return best[1]
+
+
+@pytest.mark.parametrize("dev", DEVICES[:2] + DEVICES[3:], ids=["pair152", "single152", "pair148"])
+def test_half_units_are_the_last_tiles(lib, dev):
+    """Half-width units come only from the last tiles in raster order, their
+    number matches the stated cost model, and a tile count that is a
+    multiple of the clusters gets none."""
+    for (M, N, K, L) in SHAPES + [(8192, 8192, 8192, 1), (76 * 512, 256, 4096, 1)]:
+        plan, rows = schedule(lib, dev, 0, M, N, K, L)
+        T, P = plan[3], dev[3]
+        halves = sorted({int(t) for t, wd in zip(rows[:, 3], rows[:, 6]) if wd == BN // 2})
+        assert halves == list(range(T - len(halves), T)), (M, N, K, L)
+        assert len(halves) == _model_best_halves(T, P), (M, N, K, L)
+        if T % P == 0:
+            assert not halves
+        if dev == DEVICES[0] and (M, N, K) == (8192, 8192, 8192):
+            assert (T, len(halves)) == (1024, 36)   # 988 whole tiles + 72 half units
