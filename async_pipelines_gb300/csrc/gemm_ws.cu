@@ -34,9 +34,7 @@ struct gemm_ws {
   int device;
   int num_sms;
   int cta_group;                  // 0: chosen per problem (default); 1: single-CTA tiles; 2: CTA pairs
-  int multicast;                  // 2: two CTA pairs per cluster share B by TMA multicast
   int pdl;                        // launch with programmatic stream serialisation
-  int max_quad_clusters;          // co-resident 4-CTA clusters of the multicast kernel
   int group_m;                    // raster group: m-tiles walked per n step
   int max_pair_clusters;          // co-resident 2-CTA clusters of the pair kernel
   int stream_k;                   // 0 off, 1 where the cost model gains (default), 2 always
@@ -185,26 +183,19 @@ cudaError_t max_clusters(F fn, int cs, int num_sms, uint32_t smem, int* out) {
   return cudaOccupancyMaxActiveClusters(out, fn, &cfg);
 }
 
-// Sets the shared-memory attribute of every kernel instance on the current
-// device and returns how many 2-CTA and 4-CTA clusters fit at once.
-cudaError_t configure_kernels(int num_sms, int* max_pair_clusters, int* max_quad_clusters) {
-  cudaError_t e = cudaFuncSetAttribute(gws::gemm_ws_kernel<1, 1>,
+// Sets the shared-memory attribute of both kernel instances on the current
+// device and returns how many 2-CTA clusters fit at once.
+cudaError_t configure_kernels(int num_sms, int* max_pair_clusters) {
+  cudaError_t e = cudaFuncSetAttribute(gws::gemm_ws_kernel<1>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(gws::Cfg<1, 1>::SMEM_BYTES));
+                                       static_cast<int>(gws::Cfg<1>::SMEM_BYTES));
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(gws::gemm_ws_kernel<2, 1>,
+    e = cudaFuncSetAttribute(gws::gemm_ws_kernel<2>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(gws::Cfg<2, 1>::SMEM_BYTES));
+                             static_cast<int>(gws::Cfg<2>::SMEM_BYTES));
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(gws::gemm_ws_kernel<2, 2>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(gws::Cfg<2, 2>::SMEM_BYTES));
-  if (e == cudaSuccess)
-    e = max_clusters(gws::gemm_ws_kernel<2, 1>, 2, num_sms, gws::Cfg<2, 1>::SMEM_BYTES,
+    e = max_clusters(gws::gemm_ws_kernel<2>, 2, num_sms, gws::Cfg<2>::SMEM_BYTES,
                      max_pair_clusters);
-  if (e == cudaSuccess)
-    e = max_clusters(gws::gemm_ws_kernel<2, 2>, 4, num_sms, gws::Cfg<2, 2>::SMEM_BYTES,
-                     max_quad_clusters);
   return e;
 }
 
@@ -212,9 +203,9 @@ cudaError_t configure_kernels(int num_sms, int* max_pair_clusters, int* max_quad
 constexpr int64_t kWideDMaxK = 512;
 
 // Persistent clusters the launch may use: SMs for single CTAs, else the
-// co-resident clusters of the kernel's cluster size.
+// co-resident CTA pairs.
 int64_t cluster_capacity(const gemm_ws* h, int cs) {
-  return cs == 1 ? h->num_sms : (cs == 2 ? h->max_pair_clusters : h->max_quad_clusters);
+  return cs == 1 ? h->num_sms : h->max_pair_clusters;
 }
 
 // Stream-K pieces. The tiles of a stream-K region (the last tiles in raster
@@ -277,7 +268,7 @@ struct Plan {
 // on larger ones. The handle can force either (GEMM_WS_CTA_GROUP).
 int pick_cta_group(const gemm_ws* h, int64_t M, int64_t N, int64_t K, int64_t L) {
   if (h->cta_group == 1 || h->max_pair_clusters < 1) return 1;
-  if (h->cta_group == 2 || h->multicast == 2) return 2;
+  if (h->cta_group == 2) return 2;
   const int64_t pair_tiles = L * ((M + 2 * gws::BM - 1) / (2 * gws::BM)) * ((N + gws::BN - 1) / gws::BN);
   if (K <= 512 || (K <= 1024 && pair_tiles <= 2 * static_cast<int64_t>(h->max_pair_clusters)))
     return 1;
@@ -290,11 +281,11 @@ Plan make_plan(const gemm_ws* h, int64_t M, int64_t N, int64_t K, int64_t L, boo
   Plan q;
   const int cg = pick_cta_group(h, M, N, K, L);
   q.cg = cg;
-  q.cs = cg * (cg == 2 ? h->multicast : 1);
+  q.cs = cg;
   q.tiles_m = (M + gws::BM * q.cs - 1) / (gws::BM * q.cs);
   q.tiles_n = (N + gws::BN - 1) / gws::BN;
   q.num_tiles = L * q.tiles_m * q.tiles_n;
-  const int64_t ksub = cg == 1 ? gws::Cfg<1, 1>::KSUB : gws::Cfg<2, 1>::KSUB;
+  const int64_t ksub = cg == 1 ? gws::Cfg<1>::KSUB : gws::Cfg<2>::KSUB;
   const int64_t T = q.num_tiles;
   const int64_t ns = ((K + gws::BK - 1) / gws::BK + ksub - 1) / ksub;
   q.num_stages = ns;
@@ -337,7 +328,6 @@ int launch(gemm_ws* h, const uint16_t* A, const uint16_t* B, const uint16_t* C, 
   std::memset(&p, 0, sizeof p);
   const Plan q = make_plan(h, M, N, K, L, staging != nullptr);
   const int cg = q.cg;
-  const int mc = cg == 2 ? h->multicast : 1;
   const int cs = q.cs;   // CTAs per cluster
   if (q.num_units > kMaxDim) return GEMM_WS_ERR_INVALID_ARG;
   const int64_t stn = (N + gws::STAGING - 1) / gws::STAGING;
@@ -439,27 +429,15 @@ int launch(gemm_ws* h, const uint16_t* A, const uint16_t* B, const uint16_t* C, 
     cfg.attrs = attr;
     cfg.numAttrs = nattr;
     if (cg == 1) {
-      cfg.dynamicSmemBytes = gws::Cfg<1, 1>::SMEM_BYTES;
-      e = cudaLaunchKernelEx(&cfg, gws::gemm_ws_kernel<1, 1>, p);
-    } else if (mc == 1) {
-      cfg.dynamicSmemBytes = gws::Cfg<2, 1>::SMEM_BYTES;
-      e = cudaLaunchKernelEx(&cfg, gws::gemm_ws_kernel<2, 1>, p);
+      cfg.dynamicSmemBytes = gws::Cfg<1>::SMEM_BYTES;
+      e = cudaLaunchKernelEx(&cfg, gws::gemm_ws_kernel<1>, p);
     } else {
-      cfg.dynamicSmemBytes = gws::Cfg<2, 2>::SMEM_BYTES;
-      e = cudaLaunchKernelEx(&cfg, gws::gemm_ws_kernel<2, 2>, p);
+      cfg.dynamicSmemBytes = gws::Cfg<2>::SMEM_BYTES;
+      e = cudaLaunchKernelEx(&cfg, gws::gemm_ws_kernel<2>, p);
     }
   }
   if (e != cudaSuccess) return cuda_fail(h, e);
   return GEMM_WS_OK;
-}
-
-// GEMM_WS_MULTICAST=1 makes two CTA pairs share B by TMA multicast (4-CTA
-// clusters); the default keeps one CTA pair per cluster.
-int multicast_from_env() {
-  if (const char* s = std::getenv("GEMM_WS_MULTICAST")) {
-    if (std::atoi(s) == 1) return 2;
-  }
-  return 1;
 }
 
 // GEMM_WS_PDL=0 launches without programmatic dependent launch (default on).
@@ -564,15 +542,12 @@ int gemm_ws_create(gemm_ws_t** out, int device) {
   h->encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
 
   h->cta_group = cta_group_from_env();
-  h->multicast = multicast_from_env();
   h->pdl = pdl_from_env();
   h->group_m = group_m_from_env();
   h->stream_k = stream_k_from_env();
   h->k_snake = k_snake_from_env();
-  e = configure_kernels(h->num_sms, &h->max_pair_clusters, &h->max_quad_clusters);
-  if (e == cudaSuccess && h->max_quad_clusters < 1) h->multicast = 1;
+  e = configure_kernels(h->num_sms, &h->max_pair_clusters);
   if (e == cudaSuccess && h->max_pair_clusters < 1) h->cta_group = 1;
-  if (e == cudaSuccess && h->multicast == 2 && h->cta_group == 1) h->multicast = 1;
   if (e == cudaSuccess) e = cudaMalloc(&h->work, kWorkWords * sizeof(uint32_t));
   if (e == cudaSuccess) e = cudaMemset(h->work, 0, kWorkWords * sizeof(uint32_t));
   // Stream-K workspace (see kCounterWordsPerSm).
@@ -705,21 +680,17 @@ int gemm_ws_debug_launch_shape(gemm_ws_t* h, int64_t M, int64_t N, int64_t K, in
   return GEMM_WS_OK;
 }
 
-int gemm_ws_debug_schedule(int cta_group, int multicast, int num_sms, int max_clusters,
-                           int stream_k, int64_t M, int64_t N, int64_t K, int64_t L,
-                           int streamout, int* rows, int64_t max_rows, int64_t* num_rows,
-                           int* plan) {
-  if (cta_group < 0 || cta_group > 2 || (multicast != 1 && multicast != 2) ||
-      num_sms < 1 || max_clusters < 1 || !num_rows || !plan || M <= 0 || N <= 0 || K < 0 ||
-      L <= 0 || stream_k < 0 || stream_k > 2)
+int gemm_ws_debug_schedule(int cta_group, int num_sms, int max_clusters, int stream_k,
+                           int64_t M, int64_t N, int64_t K, int64_t L, int streamout, int* rows,
+                           int64_t max_rows, int64_t* num_rows, int* plan) {
+  if (cta_group < 0 || cta_group > 2 || num_sms < 1 || max_clusters < 1 || !num_rows || !plan ||
+      M <= 0 || N <= 0 || K < 0 || L <= 0 || stream_k < 0 || stream_k > 2)
     return GEMM_WS_ERR_INVALID_ARG;
   gemm_ws h;
   std::memset(&h, 0, sizeof h);
   h.num_sms = num_sms;
   h.cta_group = cta_group;
-  h.multicast = cta_group == 2 ? multicast : 1;
   h.max_pair_clusters = max_clusters;
-  h.max_quad_clusters = max_clusters;
   if (h.cta_group == 1) h.num_sms = max_clusters;
   h.group_m = 8;
   h.stream_k = stream_k;
@@ -809,15 +780,13 @@ struct NoAllocDevice {
   bool ready;
   int num_sms;
   int cta_group;
-  int multicast;
   int max_pair_clusters;
-  int max_quad_clusters;
   uint32_t* scratch;   // device address of g_noalloc_scratch on this device
   unsigned long long timeout_ns;
   PFN_cuTensorMapEncodeTiled_v12000 encode;
 #ifdef GEMM_WS_DEBUG
-  int debug_fault;
-  unsigned long long* trace;
+  int debug_fault;                      // set by gemm_ws_debug_noalloc_configure
+  unsigned long long debug_timeout_ns;  // 0: timeout_ns
 #endif
 };
 
@@ -852,13 +821,10 @@ int noalloc_setup(int device, NoAllocDevice** out) {
                                          &q) != cudaSuccess ||
         q != cudaDriverEntryPointSuccess || !fn)
       return GEMM_WS_ERR_CUDA;
-    int pair_clusters = 0, quad_clusters = 0;
-    if (configure_kernels(sms, &pair_clusters, &quad_clusters) != cudaSuccess)
-      return GEMM_WS_ERR_CUDA;
+    int pair_clusters = 0;
+    if (configure_kernels(sms, &pair_clusters) != cudaSuccess) return GEMM_WS_ERR_CUDA;
     d.cta_group = pair_clusters >= 1 ? cta_group_from_env() : 1;
-    d.multicast = quad_clusters >= 1 ? multicast_from_env() : 1;
     d.max_pair_clusters = pair_clusters;
-    d.max_quad_clusters = quad_clusters;
     uint32_t* ptr = nullptr;
     // In host code the array's name is only a host-side stand-in; the kernel
     // must be given this device address instead.
@@ -899,14 +865,28 @@ extern "C" int gemm_ws_run_streamout_noalloc(const uint16_t* A, const uint16_t* 
   h.device = device;
   h.num_sms = d->num_sms;
   h.cta_group = d->cta_group;
-  h.multicast = d->multicast;
   h.pdl = pdl_from_env();
-  h.max_quad_clusters = d->max_quad_clusters;
   h.group_m = group_m_from_env();
   h.k_snake = k_snake_from_env();   // same schedule, hence same bits, as a handle
   h.max_pair_clusters = d->max_pair_clusters;
   h.work = d->scratch;
   h.timeout_ns = d->timeout_ns;
   h.encode = d->encode;
+#ifdef GEMM_WS_DEBUG
+  h.debug_fault = d->debug_fault;
+  if (d->debug_timeout_ns) h.timeout_ns = d->debug_timeout_ns;
+#endif
   return gemm_ws_run_streamout(&h, A, B, C, D, M, N, K, L, alpha, beta, staging, flags, stream);
 }
+
+#ifdef GEMM_WS_DEBUG
+extern "C" int gemm_ws_debug_noalloc_configure(int device, int fault, long long timeout_ms) {
+  if (device < 0 || device >= kNoAllocMaxDevices || fault < 0 || fault > 1 || timeout_ms < 0)
+    return GEMM_WS_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+  NoAllocDevice& d = g_noalloc_devices[device];
+  d.debug_fault = fault;
+  d.debug_timeout_ns = static_cast<unsigned long long>(timeout_ms) * 1000000ull;
+  return GEMM_WS_OK;
+}
+#endif

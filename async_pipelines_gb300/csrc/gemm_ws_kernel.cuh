@@ -107,15 +107,12 @@ constexpr int BAR_D_EMPTY = BAR_D_FULL + EPI_SLOTS_NOC;
 constexpr int BAR_MMA_DRAIN = BAR_D_EMPTY + EPI_SLOTS_NOC;
 constexpr int NUM_BARS = BAR_MMA_DRAIN + 1;
 
-template <int CG, int MC>
+template <int CG>
 struct Cfg {
   static_assert(CG == 1 || CG == 2, "CTA group of 1 or 2");
-  static_assert(MC == 1 || (MC == 2 && CG == 2), "B multicast across two CTA pairs only");
-  static constexpr int CS = CG * MC;                     // CTAs per cluster
+  static constexpr int CS = CG;                          // CTAs per cluster
   static constexpr int TILE_M = BM * CG;                 // rows per (pair) tile
-  static constexpr int CLUSTER_M = TILE_M * MC;          // rows per cluster tile
   static constexpr int B_ROWS = BN / CG;                 // B rows in each CTA's stage
-  static constexpr int B_LOAD_ROWS = BN / CS;            // B rows each CTA loads (whole tile)
   static constexpr uint16_t ALL_CTAS = static_cast<uint16_t>((1u << CS) - 1u);
   // 64-deep k-blocks per ring stage. The CTA pair takes two (a 128-deep
   // stage of 64 KiB, 3 stages): half the barrier round trips per MMA, which
@@ -452,14 +449,14 @@ __device__ __forceinline__ bool warp_wait_spin(uint32_t bar, uint32_t parity,
 // streams from two threads measured 2-3 % more tensor throughput per clock.
 enum ProducerPart { LOAD_A = 0, LOAD_B = 1 };
 
-template <int CG, int MC>
+template <int CG>
 __device__ __forceinline__ void producer_role(const Params& p, uint32_t sbase, uint32_t rank,
                                               ProducerPart part, const Watchdog& wd) {
-  using C = Cfg<CG, MC>;
+  using C = Cfg<CG>;
   auto full = [&](uint32_t s) { return sbase + C::OFF_BAR + 8 * (BAR_FULL + s); };
   auto empty = [&](uint32_t s) { return sbase + C::OFF_BAR + 8 * (BAR_EMPTY + s); };
   const int cluster = blockIdx.x / C::CS, clusters = gridDim.x / C::CS;
-  const int h = static_cast<int>(rank) % CG, pair = static_cast<int>(rank) / CG;
+  const int h = static_cast<int>(rank);   // CTA of the pair (0: even)
   const bool leader = part == LOAD_A && h == 0;   // arms full[s] for the pair
   uint32_t g = 0;   // stages issued by this warp so far (ring position)
   bool ok = true;
@@ -470,12 +467,7 @@ __device__ __forceinline__ void producer_role(const Params& p, uint32_t sbase, u
   for (int it = 0; ok && next_unit(p, cluster, clusters, it, w); ++it) {
     const int l = w.l;
     const int a_row = (w.mb * C::CS + static_cast<int>(rank)) * BM;   // this CTA's rows
-    // B rows of this CTA's half of the pair's N; with multicast (MC == 2) each
-    // CTA loads the pair-th quarter of that half and sends it to the CTA with
-    // the same half in every pair, at the same shared-memory offset.
-    const int b_rows = w.width / C::CS;
-    const int b_row = w.n0 + h * (w.width / CG) + pair * b_rows;
-    const uint32_t b_off = static_cast<uint32_t>(pair * b_rows) * (BK * 2);
+    const int b_row = w.n0 + h * (w.width / CG);                      // its half of the N range
     const bool whole = w.width == BN;
     const CUtensorMap* tmb = whole ? &p.tmB : &p.tmB2;
     const uint32_t tx = whole ? C::STAGE_TX : C::STAGE_TX_HALF;
@@ -485,7 +477,7 @@ __device__ __forceinline__ void producer_role(const Params& p, uint32_t sbase, u
       const int kb = w.rev ? w.kb1 - 1 - it : w.kb0 + it;
       const uint32_t s = g % C::STAGES;
       const uint32_t ph = (g / C::STAGES) & 1;
-      if (!token && !wait_spin<MC == 2>(empty(s), ph ^ 1, wd)) {
+      if (!token && !wait_spin<false>(empty(s), ph ^ 1, wd)) {
         ok = false;
         break;
       }
@@ -495,8 +487,7 @@ __device__ __forceinline__ void producer_role(const Params& p, uint32_t sbase, u
       if (leader) mbar_arrive_expect_tx(full(s), tx);
       // Both CTAs' copies complete on the pair's even CTA's full[s]. Slabs
       // past K (a ragged last stage) are zero-filled by the TMA.
-      const uint32_t full_bar =
-          CG == 1 ? full(s) : mapa_shared(full(s), static_cast<uint32_t>(pair * CG));
+      const uint32_t full_bar = CG == 1 ? full(s) : mapa_shared(full(s), 0u);
 #pragma unroll
       for (int ks = 0; ks < C::KSUB; ++ks) {
         const int k0 = (kb * C::KSUB + ks) * BK;
@@ -510,11 +501,8 @@ __device__ __forceinline__ void producer_role(const Params& p, uint32_t sbase, u
           const uint32_t bdst = sbase + C::OFF_B + s * C::B_STAGE_BYTES + ks * C::B_BLOCK_BYTES;
           if constexpr (CG == 1)
             tma_load_3d(bdst, tmb, full_bar, k0, b_row, l);
-          else if constexpr (MC == 1)
-            tma_load_3d_pair(bdst, tmb, full_bar, k0, b_row, l);
           else
-            tma_load_3d_pair_mc(bdst + b_off, tmb, full_bar, k0, b_row, l,
-                                static_cast<uint16_t>((1u << h) | (1u << (CG + h))));
+            tma_load_3d_pair(bdst, tmb, full_bar, k0, b_row, l);
         }
       }
     }
@@ -535,14 +523,12 @@ __device__ __forceinline__ void producer_role(const Params& p, uint32_t sbase, u
 
 // ------------------------------------------------------------ MMA issuer
 
-template <int CG, int MC>
+template <int CG>
 __device__ __forceinline__ void mma_role(const Params& p, uint32_t sbase, uint32_t tmem_base,
                                          uint32_t rank, const Watchdog& wd) {
-  using C = Cfg<CG, MC>;
+  using C = Cfg<CG>;
   auto bar = [&](int i) { return sbase + C::OFF_BAR + 8 * i; };
-  // Stage releases go to every CTA of the cluster (with multicast, each
-  // stage's B bytes were written by both pairs' producers); accumulator
-  // commits go to this pair's two CTAs.
+  // Stage releases and accumulator commits go to both CTAs of the pair.
   const uint16_t pair_mask = static_cast<uint16_t>(0x3u << rank);
   auto commit = [&](uint32_t b, uint16_t mask) {
     if constexpr (CG == 1)
@@ -623,11 +609,11 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
-template <int CG, int MC>
+template <int CG>
 __device__ __forceinline__ void epilogue_role(const Params& p, uint32_t sbase, uint8_t* smem,
                                               uint32_t tmem_base, uint32_t rank, int warp,
                                               const Watchdog& wd) {
-  using C = Cfg<CG, MC>;
+  using C = Cfg<CG>;
   const int lane = threadIdx.x & 31;
   const int e = warp - WARP_EPI0;    // epilogue warp 0..7
   const int q = warp & 3;            // TMEM lane quarter it may access = CTA rows 32q..32q+31
@@ -983,10 +969,10 @@ __device__ __forceinline__ void epilogue_role(const Params& p, uint32_t sbase, u
 
 // ------------------------------------------------------------ stream-out consumer
 
-template <int CG, int MC>
+template <int CG>
 __device__ __forceinline__ void consumer_role(const Params& p, uint32_t sbase, uint32_t rank,
                                               const Watchdog& wd) {
-  using C = Cfg<CG, MC>;
+  using C = Cfg<CG>;
   auto bar = [&](int i) { return sbase + C::OFF_BAR + 8 * i; };
   const int cluster = blockIdx.x / C::CS, clusters = gridDim.x / C::CS;
   // Each stream-out tile has exactly one publishing consumer, which clears
@@ -1057,9 +1043,9 @@ done:
 
 // ------------------------------------------------------------ kernel
 
-template <int CG, int MC>
+template <int CG>
 __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_ws_kernel(const __grid_constant__ Params p) {
-  using C = Cfg<CG, MC>;
+  using C = Cfg<CG>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
   const uint32_t pad = ((raw + 1023u) & ~1023u) - raw;
@@ -1079,7 +1065,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_ws_kernel(const __grid_co
     auto bar = [&](int i) { return sbase + C::OFF_BAR + 8 * i; };
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(bar(BAR_FULL + s), 1);
-      mbar_init(bar(BAR_EMPTY + s), MC);   // one MMA commit per CTA pair
+      mbar_init(bar(BAR_EMPTY + s), 1);   // one MMA commit per stage
     }
     for (int b = 0; b < ACC_BUFS; ++b) {
       mbar_init(bar(BAR_ACC_FULL + b), 1);
@@ -1134,13 +1120,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_ws_kernel(const __grid_co
 
   if (warp == WARP_TMA || warp == WARP_TMA_B) {
     if (lane == 0)
-      producer_role<CG, MC>(p, sbase, rank, warp == WARP_TMA ? LOAD_A : LOAD_B, wd);
+      producer_role<CG>(p, sbase, rank, warp == WARP_TMA ? LOAD_A : LOAD_B, wd);
   } else if (warp == WARP_MMA) {
-    if (lane == 0 && rank % CG == 0) mma_role<CG, MC>(p, sbase, tmem_base, rank, wd);
+    if (lane == 0 && rank % CG == 0) mma_role<CG>(p, sbase, tmem_base, rank, wd);
   } else if (warp < WARP_EPI0 + NUM_EPI_WARPS) {
-    epilogue_role<CG, MC>(p, sbase, smem, tmem_base, rank, warp, wd);
+    epilogue_role<CG>(p, sbase, smem, tmem_base, rank, warp, wd);
   } else if (warp == WARP_CONSUMER && p.streamout) {
-    if (lane == 0) consumer_role<CG, MC>(p, sbase, rank, wd);
+    if (lane == 0) consumer_role<CG>(p, sbase, rank, wd);
   }
 
   __syncwarp();

@@ -48,20 +48,6 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
       : "memory");
 }
 
-// Potentially-suspending probe: true once the phase of parity `parity` has
-// completed (the hardware may park the thread for a bounded time first).
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
 // Non-blocking probe (never suspends): the "try-acquire" token.
 __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
@@ -148,17 +134,6 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* m,
       : "memory");
 }
 
-// Same, with an L2 eviction-priority policy (from createpolicy).
-__device__ __forceinline__ void tma_load_3d_hint(uint32_t dst, const CUtensorMap* m,
-                                                 uint32_t bar, int x, int y, int z,
-                                                 uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
-      " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y), "r"(z), "r"(bar), "l"(policy)
-      : "memory");
-}
-
 // Tiled 3-D TMA load into this CTA's shared memory whose completion is
 // signalled on an mbarrier that may sit in the peer CTA of the pair
 // (`cluster_bar` is a shared::cluster address).
@@ -168,19 +143,6 @@ __device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap
       "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y), "r"(z), "r"(cluster_bar)
-      : "memory");
-}
-
-// Pair form with cluster multicast: the box lands at the same shared-memory
-// offset in every CTA of `cta_mask`; each destination's bytes complete on the
-// barrier at `cluster_bar`'s offset in the even CTA of that destination's pair.
-__device__ __forceinline__ void tma_load_3d_pair_mc(uint32_t dst, const CUtensorMap* m,
-                                                    uint32_t cluster_bar, int x, int y, int z,
-                                                    uint16_t cta_mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
-      " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y), "r"(z), "r"(cluster_bar), "h"(cta_mask)
       : "memory");
 }
 
@@ -246,18 +208,6 @@ __device__ __forceinline__ void red_release_gpu_add(uint32_t* p, uint32_t v) {
 
 __device__ __forceinline__ void fence_proxy_async_global() {
   asm volatile("fence.proxy.async.global;" ::: "memory");
-}
-
-__device__ __forceinline__ uint64_t policy_evict_last() {
-  uint64_t p;
-  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
-  return p;
-}
-
-__device__ __forceinline__ uint64_t policy_evict_first() {
-  uint64_t p;
-  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
-  return p;
 }
 
 __device__ __forceinline__ void st_release_gpu(uint32_t* p, uint32_t v) {

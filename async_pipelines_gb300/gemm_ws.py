@@ -82,7 +82,8 @@ def load_library(path: Optional[str] = None):
 
 
 DEBUG_EXPORTS = ("gemm_ws_debug_configure", "gemm_ws_debug_launch_shape",
-                 "gemm_ws_debug_schedule", "gemm_ws_debug_phases")
+                 "gemm_ws_debug_schedule", "gemm_ws_debug_phases",
+                 "gemm_ws_debug_noalloc_configure")
 
 _debug_lib = None
 
@@ -101,12 +102,15 @@ def load_debug_library():
         lib.gemm_ws_debug_launch_shape.restype = ctypes.c_int
         i64 = ctypes.c_int64
         lib.gemm_ws_debug_schedule.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int,
-                                               ctypes.c_int, ctypes.c_int, i64, i64, i64, i64,
+                                               ctypes.c_int, i64, i64, i64, i64,
                                                ctypes.c_int, ctypes.c_void_p, i64,
                                                ctypes.POINTER(i64), ip]
         lib.gemm_ws_debug_schedule.restype = ctypes.c_int
         lib.gemm_ws_debug_phases.argtypes = [ctypes.c_void_p, ctypes.c_void_p]
         lib.gemm_ws_debug_phases.restype = ctypes.c_int
+        lib.gemm_ws_debug_noalloc_configure.argtypes = [ctypes.c_int, ctypes.c_int,
+                                                        ctypes.c_longlong]
+        lib.gemm_ws_debug_noalloc_configure.restype = ctypes.c_int
         _debug_lib = lib
     return _debug_lib
 

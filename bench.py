@@ -659,10 +659,6 @@ def main():
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     rank, world, local = dist_env()
-    if world > 1:
-        # Cluster-multicast TMA stays in single-GPU runs: each rank's handle
-        # is created with multicast off whatever the environment says.
-        os.environ.pop("GEMM_WS_MULTICAST", None)
     if args.impl == "reference":
         run_reference(args, rank, world, local)
         return

@@ -71,11 +71,17 @@ typedef struct gemm_ws gemm_ws_t;
 /* Creates a handle bound to CUDA device `device`: checks that it is sm_103,
  * queries its SM count, allocates the device workspace and sets the kernel's
  * shared-memory attribute. The caller owns *out and frees it with
- * gemm_ws_destroy. On error *out is set to NULL. */
+ * gemm_ws_destroy. On error *out is set to NULL.
+ * Defined by: "sm90_gemm_tma_warpspecialized_cooperative.hpp", the host
+ * side of the kernel layer (`get_workspace_size` / `initialize_workspace`:
+ * the scheduler's workspace is sized and set up once, before any launch;
+ * here it lives as long as the handle). */
 int gemm_ws_create(gemm_ws_t** out, int device);
 
 /* Frees the handle and its workspace (synchronising the device first). NULL
- * is accepted and ignored. */
+ * is accepted and ignored.
+ * Defined by: the same header's workspace convention (the caller releases
+ * what initialize_workspace set up once no launch uses it). */
 int gemm_ws_destroy(gemm_ws_t* h);
 
 /* D[l] = alpha * A[l] * B[l] + beta * C[l], asynchronously on `stream`.
@@ -101,7 +107,14 @@ int gemm_ws_destroy(gemm_ws_t* h);
  * fixed for a given problem and handle (the same bits on every run): the
  * tile configuration (CTA pairs or single CTAs; GEMM_WS_CTA_GROUP=1|2 forces
  * one) and walking every other unit's K range backwards (GEMM_WS_K_SNAKE=0
- * turns that off). */
+ * turns that off).
+ * Defined by: "sm90_gemm_tma_warpspecialized_cooperative.hpp": the rank-4
+ * MNKL problem shape of `Arguments`, the `can_implement` checks, the
+ * mainloop (producer warp group loading A and B stages, consumer warp groups
+ * accumulating) and the epilogue of `operator()` (`collective_epilogue.load`
+ * of C, `collective_epilogue.store` of alpha * accumulator + beta * C);
+ * "why does load() pre-issue producer_try_acquire for the next stage": the
+ * producer ring's early try-acquire. */
 int gemm_ws_run(gemm_ws_t* h, const uint16_t* A, const uint16_t* B,
                 const uint16_t* C, uint16_t* D, int64_t M, int64_t N, int64_t K,
                 int64_t L, float alpha, float beta, void* stream);
@@ -121,7 +134,14 @@ int gemm_ws_run(gemm_ws_t* h, const uint16_t* A, const uint16_t* B,
  *    release semantics after the tile's staging bytes are globally visible.
  *    (No host-side memset: the call launches exactly one kernel.)
  *  - staging and flags must not overlap any other argument.
- * Returns as gemm_ws_run. */
+ * Returns as gemm_ws_run.
+ * Defined by: "How to build a pipeline between epilogue and communication
+ * warp groups?" (CUTLASS issue): the epilogue, as producer, acquires a
+ * buffer, stores a finished tile and commits it; a separate consumer warp
+ * waits for it, does its work on the tile and releases the buffer, while the
+ * MMA warps go on with the next tile. The issue's closing request, to show
+ * overlap and a correct handoff, is what the staging copy, sequence numbers
+ * and ready words make checkable. */
 int gemm_ws_run_streamout(gemm_ws_t* h, const uint16_t* A, const uint16_t* B,
                           const uint16_t* C, uint16_t* D, int64_t M, int64_t N,
                           int64_t K, int64_t L, float alpha, float beta,
@@ -131,7 +151,9 @@ int gemm_ws_run_streamout(gemm_ws_t* h, const uint16_t* A, const uint16_t* B,
  * GEMM_WS_OK, or GEMM_WS_ERR_TIMEOUT if a run's bounded wait gave up (the
  * run's outputs are then undefined). Reading a non-zero word clears it and
  * returns the workspace counters to zero; after a timeout, call this before
- * the next run on the handle. */
+ * the next run on the handle.
+ * Defined by: no page; every wait in the kernel is bounded (the cited
+ * kernels' waits are not), and this call reads the result of those bounds. */
 int gemm_ws_query_status(gemm_ws_t* h, void* stream);
 
 /* The last CUDA error code (cudaError_t value) seen by this handle, 0 if none. */
@@ -169,7 +191,9 @@ int64_t gemm_ws_streamout_tiles(int64_t M, int64_t N, int64_t L);
  *    GPU (e.g. on two streams) race on the counter and produce wrong sequence
  *    numbers: serialise them.
  *  - A watchdog timeout is not reported through a status query here; it shows
- *    as tiles whose ready word flags[2t+1] stayed 0. */
+ *    as tiles whose ready word flags[2t+1] stayed 0 (the kernel also records
+ *    it in a scratch word that no call reads). The next call starts from a
+ *    zero sequence counter all the same. */
 int gemm_ws_run_streamout_noalloc(const uint16_t* A, const uint16_t* B,
                                   const uint16_t* C, uint16_t* D, int64_t M,
                                   int64_t N, int64_t K, int64_t L, float alpha,

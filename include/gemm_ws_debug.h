@@ -6,7 +6,8 @@
  * The hooks serve two checks:
  *  - the watchdog: a run whose stream-out consumer warp never takes a tile
  *    must end on its own, report GEMM_WS_ERR_TIMEOUT through
- *    gemm_ws_query_status, and leave the device usable;
+ *    gemm_ws_query_status (or, for the allocation-free entry point, leave
+ *    every ready word at 0), and leave the device usable;
  *  - overlap of the tile handoff with compute, the property the issue
  *    "How to build a pipeline between epilogue and communication warp
  *    groups?" asks to be shown: per-tile global-timer stamps of "accumulator
@@ -54,7 +55,7 @@ int gemm_ws_debug_phases(gemm_ws_t* h, unsigned long long* phases);
 
 /* The launch the handle would make for an M x N x K x L problem (streamout:
  * nonzero for gemm_ws_run_streamout, 0 for gemm_ws_run): CTAs per cluster
- * (1, 2, or 4 with B multicast), number of clusters (persistent CTA groups),
+ * (1 or 2), number of clusters (persistent CTA groups),
  * an upper bound of the work-unit ids (size the trace buffer with it) and
  * the number of tiles in the stream-K region (0: every tile runs whole or
  * as two halves). Host arithmetic only.
@@ -68,7 +69,7 @@ int gemm_ws_debug_launch_shape(gemm_ws_t* h, int64_t M, int64_t N, int64_t K, in
  * or a GPU: the plan the library makes for a device with `num_sms` SMs on
  * which `max_clusters` clusters of the chosen shape fit (cta_group 1 or 2,
  * or 0 to let the library choose per problem with `max_clusters` CTA pairs
- * and `num_sms` single CTAs; multicast 1 or 2; stream_k 0 off / 1 cost
+ * and `num_sms` single CTAs; stream_k 0 off / 1 cost
  * model / 2 always), and the units
  * every cluster walks, produced by the kernel's own unit iterator.
  *  - plan[9] = {CTAs per cluster, clusters, unit-id bound, tiles, ring
@@ -79,10 +80,16 @@ int gemm_ws_debug_launch_shape(gemm_ws_t* h, int64_t M, int64_t N, int64_t K, in
  *    batch, first stage, end stage, piece, pieces, stream-K tile, cluster of
  *    piece 0, workspace slot (-1 for a whole tile)}; *num_rows = units.
  * Returns GEMM_WS_OK or GEMM_WS_ERR_INVALID_ARG. */
-int gemm_ws_debug_schedule(int cta_group, int multicast, int num_sms, int max_clusters,
-                           int stream_k, int64_t M, int64_t N, int64_t K, int64_t L,
-                           int streamout, int* rows, int64_t max_rows, int64_t* num_rows,
-                           int* plan);
+int gemm_ws_debug_schedule(int cta_group, int num_sms, int max_clusters, int stream_k,
+                           int64_t M, int64_t N, int64_t K, int64_t L, int streamout, int* rows,
+                           int64_t max_rows, int64_t* num_rows, int* plan);
+
+/* Debug state of gemm_ws_run_streamout_noalloc on CUDA device `device`, for
+ * its later calls in this process: fault 0 none, 1 the stream-out consumer
+ * warp takes no tile (as fault 1 of gemm_ws_debug_configure), so the run
+ * can only end by the watchdog; timeout_ms > 0 replaces the per-wait limit,
+ * 0 restores the default. Returns GEMM_WS_OK or GEMM_WS_ERR_INVALID_ARG. */
+int gemm_ws_debug_noalloc_configure(int device, int fault, long long timeout_ms);
 
 #ifdef __cplusplus
 }

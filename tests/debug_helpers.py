@@ -22,13 +22,11 @@ def env(**kv):
                 os.environ[k] = v
 
 
-def debug_handle(cta_group: int = 2, timeout_ms: int = 1000,
-                 multicast: int = 0) -> gemm_ws.GemmWS:
+def debug_handle(cta_group: int = 2, timeout_ms: int = 1000) -> gemm_ws.GemmWS:
     """A handle on the debug build, created with the given tile configuration
-    (CTA group, B multicast across two CTA pairs) and per-wait watchdog limit."""
+    (CTA group) and per-wait watchdog limit."""
     lib = gemm_ws.load_debug_library()
-    with env(GEMM_WS_CTA_GROUP=cta_group, GEMM_WS_TIMEOUT_MS=timeout_ms,
-             GEMM_WS_MULTICAST=multicast):
+    with env(GEMM_WS_CTA_GROUP=cta_group, GEMM_WS_TIMEOUT_MS=timeout_ms):
         return gemm_ws.GemmWS(0, lib=lib)
 
 

@@ -4,7 +4,9 @@ from __future__ import annotations
 import numpy as np
 import torch
 
+import oracle
 from async_pipelines_gb300 import workloads
+from tests.numerics import assert_gemm_close
 
 
 def bits_of(t: torch.Tensor) -> np.ndarray:
@@ -31,3 +33,17 @@ def sample_rows(M: int, L: int, n_random: int, seed: int, tile: int = 128) -> np
     rng = np.random.default_rng(seed)
     rows.update(int(r) for r in rng.integers(0, L * M, size=n_random))
     return np.array(sorted(rows), dtype=np.int64)
+
+
+def check_every_row(d_bits: np.ndarray, A, B, C, M: int, N: int, K: int, L: int,
+                    alpha: float, beta: float, what: str, chunk: int = 512):
+    """Every element of a GPU result (bf16 bits, L*M x N) against the oracle,
+    in slabs of `chunk` output rows so that the fp64 reference of a
+    full-size workload is never held whole."""
+    d_bits = np.asarray(d_bits).reshape(L * M, N)
+    Ab, Bb = bits_of(A), bits_of(B)
+    Cb = None if C is None else bits_of(C)
+    for r0 in range(0, L * M, chunk):
+        rows = np.arange(r0, min(r0 + chunk, L * M), dtype=np.int64)
+        ref = oracle.gemm_rows(Ab, Bb, Cb, M, N, K, L, alpha, beta, rows=rows)
+        assert_gemm_close(d_bits[rows], ref, K, f"{what}, rows {rows[0]}..{rows[-1]}")

@@ -23,13 +23,13 @@ from tests.test_streamout_gpu import check_staging
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("cta_group,multicast", [(2, 0), (1, 0), (2, 1)])
-def test_streamout_overlaps_mma(cta_group, multicast):
+@pytest.mark.parametrize("cta_group", [2, 1])
+def test_streamout_overlaps_mma(cta_group):
     w = workloads.WORKLOADS[workloads.STREAMOUT]
-    g = debug_handle(cta_group=cta_group, multicast=multicast)
+    g = debug_handle(cta_group=cta_group)
     cg, clusters, tiles, sk_tiles = launch_shape(g, w.M, w.N, w.K, w.L)   # cg: CTAs per cluster
     assert sk_tiles == 0
-    assert cg == cta_group * (2 if multicast else 1)
+    assert cg == cta_group
     trace = torch.zeros(tiles * cg * 2, dtype=torch.int64, device="cuda")
     configure(g, fault=0, trace_ptr=trace.data_ptr())
     A, B, _ = workloads.workload_inputs(w)

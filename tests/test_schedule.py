@@ -27,10 +27,10 @@ from async_pipelines_gb300 import gemm_ws
 
 BM, BN, BK = 128, 256, 64
 
-# (cta_group, multicast, SMs, clusters that fit): CTA pairs and single CTAs
-# on 152 and 148 SMs, and 4-CTA multicast clusters (36 fit on a 152-SM GB300).
-DEVICES = [(2, 1, 152, 76), (1, 1, 152, 152), (2, 2, 152, 36), (2, 1, 148, 74)]
-DEVICE_IDS = ["pair152", "single152", "quad152", "pair148"]
+# (cta_group, SMs, clusters that fit): CTA pairs and single CTAs on 152 and
+# 148 SMs, and CTA pairs on a GPU shared with other work (36 pairs fit).
+DEVICES = [(2, 152, 76), (1, 152, 152), (2, 152, 36), (2, 148, 74)]
+DEVICE_IDS = ["pair152", "single152", "pair152_36", "pair148"]
 
 SHAPES = [
     (256, 256, 8192, 1), (8192, 8192, 8192, 1), (4096, 4096, 4096, 1),
@@ -50,24 +50,24 @@ def lib():
 
 
 def schedule(lib, dev, stream_k, M, N, K, L, streamout=False):
-    cg, mc, sms, maxc = dev
+    cg, sms, maxc = dev
     plan = (ctypes.c_int * 9)()
     n = ctypes.c_int64()
-    rc = lib.gemm_ws_debug_schedule(cg, mc, sms, maxc, stream_k, M, N, K, L, int(streamout),
+    rc = lib.gemm_ws_debug_schedule(cg, sms, maxc, stream_k, M, N, K, L, int(streamout),
                                     None, 0, ctypes.byref(n), plan)
     assert rc == gemm_ws.OK
     rows = np.zeros((max(n.value, 1), 15), dtype=np.int32)
-    rc = lib.gemm_ws_debug_schedule(cg, mc, sms, maxc, stream_k, M, N, K, L, int(streamout),
+    rc = lib.gemm_ws_debug_schedule(cg, sms, maxc, stream_k, M, N, K, L, int(streamout),
                                     rows.ctypes.data, n.value, ctypes.byref(n), plan)
     assert rc == gemm_ws.OK
     return list(plan), rows[:n.value]
 
 
 def check(plan, rows, dev, M, N, K, L):
-    cg, mc, sms, maxc = dev
+    cg, sms, maxc = dev
     cs, clusters, id_bound, T, ns, sk_first, sk_clusters, tm, tn = plan
     ksub = 1 if cg == 1 else 2
-    assert cs == cg * (mc if cg == 2 else 1)
+    assert cs == cg
     assert tm == -(-M // (BM * cs)) and tn == -(-N // BN) and T == L * tm * tn
     assert ns == -(-(-(-K // BK)) // ksub)
     assert 1 <= clusters <= maxc
@@ -192,10 +192,10 @@ def test_tile_configuration_rule(lib, M, N, K, L, cs):
     """Default handles: single-CTA tiles for K <= 512, or K <= 1024 with at
     most two waves (2 x 76) of 256 x 256 pair tiles; CTA pairs otherwise. The
     chosen plan still covers every stage exactly once."""
-    dev = (0, 1, 152, 76)
+    dev = (0, 152, 76)
     plan, rows = schedule(lib, dev, 1, M, N, K, L)
     assert plan[0] == cs
-    check(plan, rows, (cs, 1, 152, 76 if cs == 2 else 152), M, N, K, L)
+    check(plan, rows, (cs, 152, 76 if cs == 2 else 152), M, N, K, L)
 
 
 @pytest.mark.parametrize("stream_k", [1, 2], ids=["sk_auto", "sk_always"])
@@ -205,7 +205,7 @@ def test_schedule_random_shapes(lib, stream_k):
     rule: every plan still covers every stage exactly once and keeps its
     pieces and workspace indices in bounds."""
     rng = np.random.default_rng(20261202 + stream_k)
-    devices = DEVICES + [(0, 1, 152, 76)]
+    devices = DEVICES + [(0, 152, 76)]
     for _ in range(60):
         M = int(rng.integers(1, 12000))
         N = 8 * int(rng.integers(1, 1500))
@@ -215,7 +215,7 @@ def test_schedule_random_shapes(lib, stream_k):
             plan, rows = schedule(lib, dev, stream_k, M, N, K, L)
             cs = plan[0]
             # the default rule picks per problem; check against the config it chose
-            eff = dev if dev[0] else (cs, 1, 152, 76 if cs == 2 else 152)
+            eff = dev if dev[0] else (cs, 152, 76 if cs == 2 else 152)
             check(plan, rows, eff, M, N, K, L)
 
 
@@ -241,7 +241,7 @@ def test_half_units_are_the_last_tiles(lib, dev):
     multiple of the clusters gets none."""
     for (M, N, K, L) in SHAPES + [(8192, 8192, 8192, 1), (76 * 512, 256, 4096, 1)]:
         plan, rows = schedule(lib, dev, 0, M, N, K, L)
-        T, P = plan[3], dev[3]
+        T, P = plan[3], dev[2]
         halves = sorted({int(t) for t, wd in zip(rows[:, 3], rows[:, 6]) if wd == BN // 2})
         assert halves == list(range(T - len(halves), T)), (M, N, K, L)
         assert len(halves) == _model_best_halves(T, P), (M, N, K, L)

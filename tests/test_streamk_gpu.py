@@ -30,15 +30,14 @@ from tests.numerics import assert_gemm_close, f64_to_bf16_bits
 
 pytestmark = pytest.mark.gpu
 
-CONFIGS = [(2, 0), (1, 0), (2, 1)]
-IDS = ["cta_pair", "cta_single", "cta_pair_multicast"]
+CONFIGS = [2, 1]
+IDS = ["cta_pair", "cta_single"]
 
 
-def _handle(cg, mc, stream_k, lib=None):
-    keys = ("GEMM_WS_CTA_GROUP", "GEMM_WS_MULTICAST", "GEMM_WS_STREAM_K")
+def _handle(cg, stream_k, lib=None):
+    keys = ("GEMM_WS_CTA_GROUP", "GEMM_WS_STREAM_K")
     old = {k: os.environ.get(k) for k in keys}
     os.environ["GEMM_WS_CTA_GROUP"] = str(cg)
-    os.environ["GEMM_WS_MULTICAST"] = str(mc)
     os.environ["GEMM_WS_STREAM_K"] = str(stream_k)
     try:
         return gemm_ws.GemmWS(0, lib=lib)
@@ -53,11 +52,11 @@ def _handle(cg, mc, stream_k, lib=None):
 @pytest.fixture(scope="module", params=CONFIGS, ids=IDS)
 def cfg(request):
     """(auto handle, forced handle, debug handles for their plans)."""
-    cg, mc = request.param
-    auto, forced = _handle(cg, mc, 1), _handle(cg, mc, 2)
+    cg = request.param
+    auto, forced = _handle(cg, 1), _handle(cg, 2)
     lib = gemm_ws.load_debug_library()
-    plan_auto = _handle(cg, mc, 1, lib)
-    plan_forced = _handle(cg, mc, 2, lib)
+    plan_auto = _handle(cg, 1, lib)
+    plan_forced = _handle(cg, 2, lib)
     yield auto, forced, plan_auto, plan_forced
     for g in (auto, forced):
         assert g.query_status() == gemm_ws.OK

@@ -25,7 +25,7 @@ pytestmark = pytest.mark.gpu
 
 @pytest.fixture(scope="module")
 def auto_debug():
-    keys = ("GEMM_WS_CTA_GROUP", "GEMM_WS_MULTICAST", "GEMM_WS_STREAM_K")
+    keys = ("GEMM_WS_CTA_GROUP", "GEMM_WS_STREAM_K")
     old = {k: os.environ.pop(k, None) for k in keys}
     try:
         g = gemm_ws.GemmWS(0, lib=gemm_ws.load_debug_library())

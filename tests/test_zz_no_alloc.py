@@ -8,10 +8,14 @@ passes alone in a fresh process as well.
 """
 from __future__ import annotations
 
+import ctypes
+import time
+
 import numpy as np
 import pytest
 import torch
 
+import oracle
 from async_pipelines_gb300 import gemm_ws, workloads
 from tests.gpu_helpers import bits_of
 from tests.numerics import assert_gemm_close, bf16_bits_to_f64
@@ -58,3 +62,43 @@ def test_noalloc_rejects_bad_arguments_without_launching():
     assert rc == gemm_ws.ERR_INVALID_ARG
     torch.cuda.synchronize()
     assert torch.all(D == 4.0)
+
+
+def test_noalloc_timeout_shows_as_unflagged_tiles_then_recovers():
+    """A caller of the allocation-free entry point has no handle to query, so
+    a watchdog timeout must show in the flags: with the debug build's fault
+    (the stream-out consumer takes no tile, so the epilogue waits for a slot
+    that is never released) the call ends on its own, every ready word is 0,
+    and the next two normal calls are correct."""
+    lib = gemm_ws.load_debug_library()
+    dev = torch.cuda.current_device()
+    M, N, K, L = 4096, 4096, 64, 1
+    A, B, _ = workloads.make_inputs(M, N, K, L, ("uniform",), None, seed=47)
+    Ad, Bd = A.cuda(), B.cuda()
+    T = gemm_ws.gemm_ws_streamout_tiles(M, N, L)
+    D = torch.empty(L, M, N, dtype=torch.bfloat16, device="cuda")
+    staging = torch.empty(T * 128 * 128, dtype=torch.bfloat16, device="cuda")
+    flags = torch.full((2 * T,), 0x5A5A5A5A, dtype=torch.int32, device="cuda")
+    stream = torch.cuda.current_stream().cuda_stream
+
+    def call():
+        return lib.gemm_ws_run_streamout_noalloc(
+            Ad.data_ptr(), Bd.data_ptr(), None, D.data_ptr(), M, N, K, L, 1.0, 0.0,
+            staging.data_ptr(), flags.data_ptr(), ctypes.c_void_p(stream))
+
+    assert lib.gemm_ws_debug_noalloc_configure(dev, 1, 200) == gemm_ws.OK
+    try:
+        t0 = time.perf_counter()
+        assert call() == gemm_ws.OK
+        torch.cuda.synchronize()
+        assert time.perf_counter() - t0 < 20.0
+        assert int(flags[1::2].ne(0).sum().item()) == 0    # no tile flagged ready
+    finally:
+        assert lib.gemm_ws_debug_noalloc_configure(dev, 0, 0) == gemm_ws.OK
+    ref = oracle.gemm(bits_of(A), bits_of(B), None, M, N, K, L, 1.0, 0.0)
+    for n in range(2):
+        D.fill_(float("nan"))
+        assert call() == gemm_ws.OK
+        torch.cuda.synchronize()
+        assert_gemm_close(bits_of(D), ref, K, f"no-alloc call {n} after the timeout")
+        check_staging(D, staging, flags)
