@@ -2,6 +2,10 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
+With --gpus N > 1 and no outer launcher (no WORLD_SIZE in the environment)
+the script starts N rank processes itself, one per GPU; under torchrun it
+uses the launcher's ranks.
+
 One step = one GEMM D = alpha*A*B + beta*C over the 8192^3 workload (A, B
 uniform[-1,1), C normal(0,1), alpha 1.5, beta 0.5), inputs resident in HBM.
 Every step's inputs (512 MiB) exceed the 129 MB L2, so L2 is not flushed.
@@ -10,8 +14,10 @@ Printed (rank 0, one JSON line): whole-job TFLOP/s (all ranks; replicas on N
 GPUs, weak scaling), the fraction of the measured dense bf16 peak, the
 end-to-end figure through the C ABI with host buffers, the stream-out
 overhead on the 8192 x 8192 x 4096 workload, the roofline record of the GEMM
-kernel, SM clocks sampled during the timed region, and the CPU oracle timed
-on a bounded sample of the same workload on this host's cores.
+kernel, SM clocks sampled during the timed region, a fixed-length sustained
+leg (back-to-back launches for at least half a second, under the power cap,
+with its own clock record), and the CPU oracle timed on a bounded sample of
+the same workload on this host's cores.
 
 `--impl reference` times that CPU oracle as the reference arm.
 """
@@ -20,7 +26,9 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
+import math
 import os
+import socket
 import statistics
 import subprocess
 import sys
@@ -41,6 +49,8 @@ NOMINAL_BF16_TFLOPS = 2250.0
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 # Timed regions at least this long are compared with the sustained peak.
 SUSTAINED_MIN_S = 0.25
+# Length of the sustained leg: back-to-back launches timed as one region.
+SUSTAINED_LEG_S = 0.6
 KERNEL_SOURCES = ["async_pipelines_gb300/csrc/gemm_ws.cu",
                   "async_pipelines_gb300/csrc/gemm_ws_kernel.cuh",
                   "async_pipelines_gb300/csrc/ptx.cuh"]
@@ -83,6 +93,51 @@ def dist_env():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     return rank, world, local
+
+
+def _free_port() -> int:
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_process(rank: int, world: int, port: int, argv, target):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank),
+                      LOCAL_WORLD_SIZE=str(world))
+    (target or main)(argv)
+
+
+def spawn_ranks(world: int, argv, target=None, timeout_s: float = 3600.0) -> int:
+    """Runs `target(argv)` (default: this script's main) in `world` fresh
+    processes on this node, rank r with RANK = LOCAL_RANK = r and a
+    rendezvous on 127.0.0.1, as torchrun would. Returns the worst exit code."""
+    import torch.multiprocessing as mp
+    ctx = mp.get_context("spawn")
+    port = _free_port()
+    procs = [ctx.Process(target=_rank_process, args=(r, world, port, argv, target))
+             for r in range(world)]
+    for p in procs:
+        p.start()
+    deadline = time.monotonic() + timeout_s
+    for p in procs:
+        p.join(timeout=max(1.0, deadline - time.monotonic()))
+    codes = []
+    for p in procs:
+        if p.is_alive():   # a rank that never finished: stop it, report failure
+            p.terminate()
+            p.join(timeout=10)
+            codes.append(1)
+        else:
+            codes.append(p.exitcode or 0)
+    return max(codes)
+
+
+def init_ranks(world: int):
+    """Process group of the replicas: NCCL between GPUs, gloo without CUDA."""
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
 
 
 def barrier(world):
@@ -410,6 +465,18 @@ def run_ours(args, rank, world, local):
         raise RuntimeError(f"device status after timing: {gemm_ws.status_string(status)}")
     tflops_rank = w.flops / (ms * 1e-3) / 1e12
     value = job_throughput(w.flops, world, ms)
+    # Sustained leg: a fixed length of back-to-back launches (independent of
+    # --steps) timed as one region, in the power-capped steady state that a
+    # user of long GEMM streams sees, with its own clock record.
+    n_sus = max(50, math.ceil(SUSTAINED_LEG_S / (ms * 1e-3)))
+    barrier(world)
+    with ClockSampler(local) as sus_clocks:
+        torch.cuda.synchronize()
+        ms_sus = max_over_ranks(time_launches(step, n_sus, stream), world)
+    sustained = {"launches": n_sus, "seconds": round(n_sus * ms_sus * 1e-3, 3),
+                 "ms_per_launch": round(ms_sus, 4),
+                 "tflops": round(job_throughput(w.flops, world, ms_sus), 2),
+                 "clocks": sus_clocks.summary()}
     # Informational: 20 single launches, each timed alone (events around one
     # call, synchronised between calls), median and best.
     singles = sorted(time_launches(step, 1, stream) for _ in range(20))
@@ -476,6 +543,9 @@ def run_ours(args, rank, world, local):
     timed_s = ms * args.steps / 1e3
     regime = "sustained" if timed_s >= SUSTAINED_MIN_S else "burst"
     roof_peak = peak_sus if regime == "sustained" else peak
+    sustained["peak_sustained"] = peak_sus
+    sustained["frac_of_sustained"] = round(
+        w.flops / (sustained["ms_per_launch"] * 1e-3) / 1e12 / peak_sus, 4)
     cpu = None
     if not args.no_cpu_baseline:
         sampler = OracleSampler(w)
@@ -502,6 +572,7 @@ def run_ours(args, rank, world, local):
         "pct_of_nominal_2250_tflops": round(100.0 * tflops_rank / NOMINAL_BF16_TFLOPS, 2),
         "pct_of_measured_bf16_burst": round(100.0 * tflops_rank / peak, 2),
         "single_launch": single,
+        "sustained": sustained,
         "streamout_overhead_pct": round(overhead, 2),
         "streamout": {"workload": so.name, "plain_ms_median": round(mp, 4),
                       "streamout_ms_median": round(ms_so, 4), "reps": len(t_plain),
@@ -635,7 +706,7 @@ def run_reference(args, rank, world, local):
     print(json.dumps(line), flush=True)
 
 
-def main():
+def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=1000)
@@ -655,9 +726,12 @@ def main():
                     help="interleaved rounds against torch.addmm (cuBLAS) on the headline "
                          "workload; a cross-check, no contract line")
     ap.add_argument("--rounds", type=int, default=6)
-    args = ap.parse_args()
+    args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        # No outer launcher: start one rank per GPU here.
+        sys.exit(spawn_ranks(args.gpus, sys.argv[1:] if argv is None else argv))
     rank, world, local = dist_env()
     if args.impl == "reference":
         run_reference(args, rank, world, local)
@@ -669,9 +743,8 @@ def main():
         run_vs_library(args, local)
         return
     if world > 1:
-        import torch.distributed as dist
         torch.cuda.set_device(local)
-        dist.init_process_group("nccl")
+    init_ranks(world)
     try:
         run_ours(args, rank, world, local)
     finally:
