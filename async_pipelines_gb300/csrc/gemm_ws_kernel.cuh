@@ -609,6 +609,95 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
+// Epilogue of a launch with wide D stores (short K, beta == 0, no stream-out,
+// no split pieces): D leaves in 32 x 64 blocks (128-byte rows, 128-byte
+// swizzle), half the TMA store rows of 32 x 32 blocks, which is what bounds a
+// short-K GEMM's epilogue. Warp (q, hf) takes the unit's 64-column blocks jw
+// with jw % 2 == hf through its own 4 KiB area of the epilogue region (laid
+// out differently from the D slots, so a launch never mixes the two); one
+// block in flight per warp. A loop of its own, apart from the general
+// epilogue's: measured 2.7 % faster on 8192 x 8192 x 64 than the same steps
+// as one branch of the general loop.
+template <int CG>
+__device__ __forceinline__ void epilogue_wide(const Params& p, uint32_t sbase, uint8_t* smem,
+                                              uint32_t tmem_base, uint32_t rank, int warp,
+                                              const Watchdog& wd) {
+  using C = Cfg<CG>;
+  const int lane = threadIdx.x & 31;
+  const int e = warp - WARP_EPI0;
+  const int q = warp & 3;
+  const int hf = e / EPI_HALF_WARPS;
+  auto bar = [&](int i) { return sbase + C::OFF_BAR + 8 * i; };
+  const int cluster = blockIdx.x / C::CS, clusters = gridDim.x / C::CS;
+  uint8_t* dq = smem + C::OFF_D + hf * (4 * WIDE_QUARTER_BYTES) + q * WIDE_QUARTER_BYTES;
+  const uint32_t wrow = lane * 128, wswz = lane & 7;
+  int i = 0;
+  Unit w;
+  for (; next_unit(p, cluster, clusters, i, w); ++i) {
+    const int l = w.l;
+    const int row_tile = w.mb * C::CS + static_cast<int>(rank);
+    const int m0 = row_tile * BM + 32 * q, n0 = w.n0;
+    const int nwide = staging_in_part(p, row_tile, w) * (STAGING / (2 * EPI_N));   // 0, 2 or 4
+    const uint32_t b = i & 1, aph = (i >> 1) & 1;
+    const bool has_acc = w.kb1 > w.kb0;
+    auto release_acc = [&]() {
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) {
+        if (CG == 1 || rank % CG == 0)
+          mbar_arrive(bar(BAR_ACC_EMPTY + b));
+        else
+          mbar_arrive_cluster(mapa_shared(bar(BAR_ACC_EMPTY + b), rank - rank % CG));
+      }
+    };
+    if (!warp_wait_spin(bar(BAR_ACC_FULL + b), aph, wd)) break;
+    tc_fence_after_sync();
+#ifdef GEMM_WS_DEBUG
+    if (p.trace && q == (WARP_EPI0 & 3) && hf == 0 && lane == 0)
+      p.trace[(static_cast<size_t>(w.id) * C::CS + rank) * 2] = global_timer_ns();
+#endif
+    const uint32_t tacc = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + b * BN;
+    if (nwide == 0) release_acc();   // this CTA's rows lie outside M x N
+    for (int jw = hf; jw < nwide; jw += 2) {
+      uint32_t a0[32], a1[32];
+      if (has_acc) {
+        tmem_ld_32x32b_x32(tacc + (2 * jw) * EPI_N, a0);
+        tmem_ld_32x32b_x32(tacc + (2 * jw + 1) * EPI_N, a1);
+        tmem_wait_ld();
+      } else {
+#pragma unroll
+        for (int x = 0; x < 32; ++x) a0[x] = a1[x] = 0u;
+      }
+      if (jw + 2 >= nwide) release_acc();
+      if (lane == 0) bulk_wait_read<0>();   // this warp's previous block has been read
+      __syncwarp();
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        const uint32_t* a = c < 4 ? a0 : a1;
+        const int o = 8 * (c & 3);
+        uint4 wv;
+        wv.x = pack_bf16x2(p.alpha * __uint_as_float(a[o + 0]), p.alpha * __uint_as_float(a[o + 1]));
+        wv.y = pack_bf16x2(p.alpha * __uint_as_float(a[o + 2]), p.alpha * __uint_as_float(a[o + 3]));
+        wv.z = pack_bf16x2(p.alpha * __uint_as_float(a[o + 4]), p.alpha * __uint_as_float(a[o + 5]));
+        wv.w = pack_bf16x2(p.alpha * __uint_as_float(a[o + 6]), p.alpha * __uint_as_float(a[o + 7]));
+        *reinterpret_cast<uint4*>(dq + wrow + ((c ^ wswz) << 4)) = wv;
+      }
+      fence_proxy_async_smem();   // generic writes -> visible to the TMA (async proxy)
+      __syncwarp();
+      if (lane == 0) {
+        tma_store_3d(&p.tmDw, smem_addr(dq), n0 + jw * 2 * EPI_N, m0, l);
+        bulk_commit();
+      }
+    }
+#ifdef GEMM_WS_DEBUG
+    if (p.trace && q == (WARP_EPI0 & 3) && hf == 0 && lane == 0)
+      p.trace[(static_cast<size_t>(w.id) * C::CS + rank) * 2 + 1] = global_timer_ns();
+#endif
+  }
+  if (lane == 0) bulk_wait_read<0>();   // store tail: shared memory read before the CTA exits
+  __syncwarp();
+}
+
 template <int CG>
 __device__ __forceinline__ void epilogue_role(const Params& p, uint32_t sbase, uint8_t* smem,
                                               uint32_t tmem_base, uint32_t rank, int warp,
@@ -628,7 +717,6 @@ __device__ __forceinline__ void epilogue_role(const Params& p, uint32_t sbase, u
   // read, its buffers take the space) or two.
   const uint32_t per_half = (p.has_c ? EPI_SLOTS : EPI_SLOTS_NOC) / 2;
   const uint32_t cbuf = sbase + C::OFF_C + static_cast<uint32_t>(e) * EPI_QUARTER_BYTES;
-  const bool wide = p.wide_d != 0;
   const uint32_t cbar = bar(BAR_C_FULL + e);
   uint32_t u = 0;        // subtiles stored by this warp (slot ring position)
   uint32_t cu = 0;       // C subtiles consumed by this warp
@@ -722,7 +810,7 @@ __device__ __forceinline__ void epilogue_role(const Params& p, uint32_t sbase, u
     const bool split = w.pieces > 1;
     if (p.has_c && nsub > 0 && !split) issue_c(hf);
 
-    if (!warp_wait(bar(BAR_ACC_FULL + b), aph, wd)) break;
+    if (!warp_wait_spin(bar(BAR_ACC_FULL + b), aph, wd)) break;
     tc_fence_after_sync();
 #ifdef GEMM_WS_DEBUG
     // stamp 0: this CTA's part of the unit has its accumulator (MMA done)
@@ -732,51 +820,7 @@ __device__ __forceinline__ void epilogue_role(const Params& p, uint32_t sbase, u
     const uint32_t tacc = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + b * BN;
 
     bool ok = true;
-    if (wide) {
-      // Short K, without C, stream-out or split pieces in the launch: D goes
-      // out in 32 x 64 blocks (128-byte rows, 128-byte swizzle), half the
-      // TMA store rows of 32 x 32 blocks, which is what bounds a short-K
-      // GEMM's epilogue. Warp (q, hf) takes the unit's 64-column blocks jw
-      // with jw % 2 == hf through its own 4 KiB area of the epilogue region
-      // (laid out differently from the D slots, so a launch never mixes the
-      // two). One block in flight per warp: with longer K, where the
-      // epilogue hides under the MMA, the narrow path's two are better.
-      if (nsub == 0) release_acc();
-      const int nwide = nsub / 2;
-      uint8_t* dq = smem + C::OFF_D + hf * (4 * WIDE_QUARTER_BYTES) + q * WIDE_QUARTER_BYTES;
-      const uint32_t wrow = lane * 128, wswz = lane & 7;
-      for (int jw = hf; jw < nwide; jw += 2) {
-        uint32_t a0[32], a1[32];
-        if (has_acc) {
-          tmem_ld_32x32b_x32(tacc + (2 * jw) * EPI_N, a0);
-          tmem_ld_32x32b_x32(tacc + (2 * jw + 1) * EPI_N, a1);
-          tmem_wait_ld();
-        } else {
-#pragma unroll
-          for (int x = 0; x < 32; ++x) a0[x] = a1[x] = 0u;
-        }
-        if (jw + 2 >= nwide) release_acc();
-        if (lane == 0) bulk_wait_read<0>();   // this warp's previous block has been read
-        __syncwarp();
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          const uint32_t* a = c < 4 ? a0 : a1;
-          const int o = 8 * (c & 3);
-          uint4 wv;
-          wv.x = pack_bf16x2(p.alpha * __uint_as_float(a[o + 0]), p.alpha * __uint_as_float(a[o + 1]));
-          wv.y = pack_bf16x2(p.alpha * __uint_as_float(a[o + 2]), p.alpha * __uint_as_float(a[o + 3]));
-          wv.z = pack_bf16x2(p.alpha * __uint_as_float(a[o + 4]), p.alpha * __uint_as_float(a[o + 5]));
-          wv.w = pack_bf16x2(p.alpha * __uint_as_float(a[o + 6]), p.alpha * __uint_as_float(a[o + 7]));
-          *reinterpret_cast<uint4*>(dq + wrow + ((c ^ wswz) << 4)) = wv;
-        }
-        fence_proxy_async_smem();   // generic writes -> visible to the TMA (async proxy)
-        __syncwarp();
-        if (lane == 0) {
-          tma_store_3d(&p.tmDw, smem_addr(dq), n0 + jw * 2 * EPI_N, m0, l);
-          bulk_commit();
-        }
-      }
-    } else if (!split) {
+    if (!split) {
       if (nsub == 0) release_acc();   // this CTA's rows lie outside M x N
       for (int j = hf; j < nsub; j += 2) {
         uint32_t acc[32];
@@ -1124,7 +1168,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_ws_kernel(const __grid_co
   } else if (warp == WARP_MMA) {
     if (lane == 0 && rank % CG == 0) mma_role<CG>(p, sbase, tmem_base, rank, wd);
   } else if (warp < WARP_EPI0 + NUM_EPI_WARPS) {
-    epilogue_role<CG>(p, sbase, smem, tmem_base, rank, warp, wd);
+    if (p.wide_d)
+      epilogue_wide<CG>(p, sbase, smem, tmem_base, rank, warp, wd);
+    else
+      epilogue_role<CG>(p, sbase, smem, tmem_base, rank, warp, wd);
   } else if (warp == WARP_CONSUMER && p.streamout) {
     if (lane == 0) consumer_role<CG>(p, sbase, rank, wd);
   }
