@@ -250,7 +250,8 @@ struct Plan {
   int cg;              // CTA group of the MMA (1 or 2)
   int cs;              // CTAs per cluster
   int64_t tiles_m, tiles_n, num_tiles;
-  int64_t num_full;    // whole-width units (the rest of the tiles run as halves)
+  int64_t num_full;    // whole-width units (the rest of the tiles run as `split` parts)
+  int64_t split;       // 2: halves, 4: quarters
   int64_t num_units;   // units (an upper bound of unit ids with stream-K)
   int64_t num_stages;  // ring stages covering K
   int64_t sk_first;    // first tile of the stream-K region (num_tiles: none)
@@ -292,26 +293,40 @@ Plan make_plan(const gemm_ws* h, int64_t M, int64_t N, int64_t K, int64_t L, boo
   const int64_t P = cluster_capacity(h, q.cs);
   double dp_cost = 0.0;
   q.num_full = choose_num_full(T, P, &dp_cost);
+  q.split = 2;
   q.num_units = q.num_full + 2 * (T - q.num_full);
   q.clusters = q.num_units < P ? q.num_units : P;
   q.sk_first = T;
   q.sk_split = 1;
   q.sk_clusters = 0;
+  // Quarter units for problems of so few tiles that four units per tile fit
+  // on the GPU at once (a latency-bound launch: each SM's loads, MMAs and
+  // epilogue shrink with the unit), unless split pieces are taken below.
+  // Stream-out keeps its 128-column handoff granularity, so no quarters.
+  auto quarters = [&](Plan& r) {
+    if (!streamout && 4 * T <= P) {
+      r.num_full = 0;
+      r.split = 4;
+      r.num_units = 4 * T;
+      r.clusters = r.num_units;
+    }
+    return r;
+  };
   // Stream-out keeps whole tiles: its consumer takes every tile where the
   // epilogue computes it.
-  if (streamout || h->stream_k == 0 || !h->partial || P < 2) return q;
+  if (streamout || h->stream_k == 0 || !h->partial || P < 2) return quarters(q);
   const bool forced = h->stream_k == 2;
   const int64_t min_share = forced ? 1 : kMinShareK / (gws::BK * ksub);
   const int64_t R = 2 * T <= P ? T : T % P;   // tiles of the stream-K region
-  if (R == 0 || 2 * R > P) return q;
+  if (R == 0 || 2 * R > P) return quarters(q);
   int64_t S = P / R;
   if (S > ns / min_share) S = ns / min_share;
   if (S > (forced ? kMaxSplitForced : kMaxSplit)) S = forced ? kMaxSplitForced : kMaxSplit;
-  if (S < 2) return q;
+  if (S < 2) return quarters(q);
   const int64_t F = T - R, Pe = R * S;
   const double sk_cost = static_cast<double>(F / P) + static_cast<double>((ns + S - 1) / S) / ns +
                          kPieceCostStages / static_cast<double>(ns);
-  if (!forced && !(sk_cost < dp_cost - 1e-9)) return q;
+  if (!forced && !(sk_cost < dp_cost - 1e-9)) return quarters(q);
   q.sk_first = F;
   q.sk_split = S;
   q.sk_clusters = Pe;
@@ -341,9 +356,10 @@ int launch(gemm_ws* h, const uint16_t* A, const uint16_t* B, const uint16_t* C, 
     if (r == CUDA_SUCCESS)
       r = encode3d(h, &p.tmB, B, K, N, L, gws::BK, gws::BN / cs, CU_TENSOR_MAP_SWIZZLE_128B,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
-    if (r == CUDA_SUCCESS)
-      r = encode3d(h, &p.tmB2, B, K, N, L, gws::BK, gws::BN / 2 / cs,
-                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+    if (r == CUDA_SUCCESS && q.num_full < q.num_tiles)
+      r = encode3d(h, q.split == 4 ? &p.tmB4 : &p.tmB2, B, K, N, L, gws::BK,
+                   static_cast<uint32_t>(gws::BN / q.split / cs), CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
   }
   if (r == CUDA_SUCCESS && beta != 0.0f)
     r = encode3d(h, &p.tmC, C, N, M, L, gws::EPI_N, 32, CU_TENSOR_MAP_SWIZZLE_64B,
@@ -375,6 +391,7 @@ int launch(gemm_ws* h, const uint16_t* A, const uint16_t* B, const uint16_t* C, 
   p.tiles_n = static_cast<int>(q.tiles_n);
   p.num_tiles = static_cast<int>(q.num_tiles);
   p.num_full = static_cast<int>(q.num_full);
+  p.split = static_cast<int>(q.split);
   p.num_units = static_cast<int>(q.num_units);
   p.num_kb = static_cast<int>((K + gws::BK - 1) / gws::BK);
   p.num_stages = static_cast<int>(q.num_stages);
@@ -707,6 +724,7 @@ int gemm_ws_debug_schedule(int cta_group, int num_sms, int max_clusters, int str
   p.tiles_n = static_cast<int>(q.tiles_n);
   p.num_tiles = static_cast<int>(q.num_tiles);
   p.num_full = static_cast<int>(q.num_full);
+  p.split = static_cast<int>(q.split);
   p.num_units = static_cast<int>(q.num_units);
   p.num_stages = static_cast<int>(q.num_stages);
   p.sk_first = static_cast<int>(q.sk_first);

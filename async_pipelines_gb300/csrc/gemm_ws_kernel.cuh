@@ -125,6 +125,7 @@ struct Cfg {
   static constexpr uint32_t B_STAGE_BYTES = KSUB * B_BLOCK_BYTES; // B part of a stage
   static constexpr uint32_t STAGE_TX = CG * (A_BYTES + B_STAGE_BYTES);
   static constexpr uint32_t STAGE_TX_HALF = CG * (A_BYTES + B_STAGE_BYTES / 2);
+  static constexpr uint32_t STAGE_TX_QUARTER = CG * (A_BYTES + B_STAGE_BYTES / 4);
   // Shared-memory carve-out (offsets from a 1024-byte aligned base).
   static constexpr uint32_t OFF_A = 0;
   static constexpr uint32_t OFF_B = OFF_A + STAGES * A_BYTES;
@@ -140,6 +141,7 @@ struct Cfg {
   static constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;   // + slack to align the base
   static constexpr uint32_t IDESC = idesc_bf16_f32(TILE_M, BN);
   static constexpr uint32_t IDESC_HALF = idesc_bf16_f32(TILE_M, BN / 2);
+  static constexpr uint32_t IDESC_QUARTER = idesc_bf16_f32(TILE_M, BN / 4);
   static_assert(STAGES <= NUM_STAGES_MAX, "barrier table");
   static_assert(OFF_B + STAGES * B_STAGE_BYTES - OFF_A >= NUM_EPI_WARPS * RED_AREA_BYTES,
                 "the split-K reduction stages partials in the operand ring");
@@ -151,13 +153,15 @@ struct Params {
   CUtensorMap tmA;   // {K, M, L}, box {64, 128}, 128-byte swizzle
   CUtensorMap tmB;   // {K, N, L}, box {64, 256 / CG}, 128-byte swizzle
   CUtensorMap tmB2;  // {K, N, L}, box {64, 128 / CG}: B of a half-width unit
+  CUtensorMap tmB4;  // {K, N, L}, box {64, 64 / CG}: B of a quarter-width unit
   CUtensorMap tmC;   // {N, M, L}, box {32, 32},  64-byte swizzle (beta != 0)
   CUtensorMap tmD;   // {N, M, L}, box {32, 32},  64-byte swizzle
   CUtensorMap tmDw;  // {N, M, L}, box {64, 32}, 128-byte swizzle (wide stores)
   CUtensorMap tmS;   // staging {128, 128, T}, box {32, 128}, 64-byte swizzle
   int M, N, K, L;
   int tiles_m, tiles_n, num_tiles, num_kb;   // tiles of 128*CG x 256
-  int num_full;                  // tiles [0, num_full) run whole; the rest as two halves
+  int num_full;                  // tiles [0, num_full) run whole; the rest as `split` parts
+  int split;                     // 2: halves (128 columns), 4: quarters (64 columns)
   int num_units;                 // work units (see unit_coords)
   int num_stages;                // ring stages covering K (KSUB k-blocks each)
   // Stream-K: the K ranges of tiles [sk_first, num_tiles) are cut into
@@ -207,11 +211,13 @@ __host__ __device__ __forceinline__ void tile_coords(const Params& p, int t, int
 
 // A unit of work: a tile (256 columns, or, for the last tiles in raster
 // order, one 128-column half, so that the final wave of the persistent
-// schedule is not left half idle), or a piece of a tile's K range.
+// schedule is not left half idle; or, in a problem of so few tiles that four
+// units per tile fit on the GPU at once, one 64-column quarter), or a piece
+// of a tile's K range.
 struct Unit {
   int mb, l;
   int n0;      // first column
-  int width;   // 256 or 128 columns
+  int width;   // 256, 128 or 64 columns
   int tile;    // tile index
   int kb0, kb1;        // ring stages [kb0, kb1) of the tile's K range
   int piece, pieces;   // piece `piece` of the `pieces` that share the K range (1: whole)
@@ -240,13 +246,14 @@ __host__ __device__ __forceinline__ Unit whole_tile(const Params& p, int t) {
 }
 
 // Without stream-K: unit u < num_full is tile u; the units after it are the
-// halves of the remaining tiles.
+// halves (split == 2) or quarters (split == 4) of the remaining tiles.
 __host__ __device__ __forceinline__ Unit unit_coords(const Params& p, int u) {
   if (u < p.num_full) return whole_tile(p, u);
   const int h = u - p.num_full;
-  Unit w = whole_tile(p, p.num_full + (h >> 1));
-  w.n0 += (h & 1) ? BN / 2 : 0;
-  w.width = BN / 2;
+  const int lg = p.split == 4 ? 2 : 1;
+  Unit w = whole_tile(p, p.num_full + (h >> lg));
+  w.width = BN >> lg;
+  w.n0 += (h & (p.split - 1)) * w.width;
   w.id = u;
   return w;
 }
@@ -296,10 +303,20 @@ __host__ __device__ __forceinline__ bool next_unit(const Params& p, int c, int c
 
 // Stream-out tiles (128 x 128) of this CTA's 128-row part of a unit that
 // exist inside M x N: 0, 1 or 2. Epilogue and consumer use the same count.
+// (Stream-out launches have no quarter units.)
 __device__ __forceinline__ int staging_in_part(const Params& p, int row_tile, const Unit& w) {
   if (row_tile >= p.staging_tiles_m || w.n0 >= p.N) return 0;
   const int cols_left = p.N - w.n0;
   return min(w.width / STAGING, (cols_left + STAGING - 1) / STAGING);
+}
+
+// 32-column subtiles the epilogue stores for this CTA's 128-row part of a
+// unit: the part's columns inside N, rounded up to whole 128-column blocks
+// (the TMA stores clip at N), at most the unit's width: 0, 2, 4 or 8.
+__device__ __forceinline__ int subtiles_in_part(const Params& p, int row_tile, const Unit& w) {
+  if (row_tile >= p.staging_tiles_m || w.n0 >= p.N) return 0;
+  const int cols = ((p.N - w.n0 + STAGING - 1) / STAGING) * STAGING;
+  return min(w.width, cols) / EPI_N;
 }
 
 struct Watchdog {
@@ -468,9 +485,10 @@ __device__ __forceinline__ void producer_role(const Params& p, uint32_t sbase, u
     const int l = w.l;
     const int a_row = (w.mb * C::CS + static_cast<int>(rank)) * BM;   // this CTA's rows
     const int b_row = w.n0 + h * (w.width / CG);                      // its half of the N range
-    const bool whole = w.width == BN;
-    const CUtensorMap* tmb = whole ? &p.tmB : &p.tmB2;
-    const uint32_t tx = whole ? C::STAGE_TX : C::STAGE_TX_HALF;
+    const CUtensorMap* tmb = w.width == BN ? &p.tmB : (w.width == BN / 2 ? &p.tmB2 : &p.tmB4);
+    const uint32_t tx = w.width == BN       ? C::STAGE_TX
+                        : w.width == BN / 2 ? C::STAGE_TX_HALF
+                                            : C::STAGE_TX_QUARTER;
     for (int it = 0; it < w.kb1 - w.kb0; ++it) {
       // With k_snake, odd units walk K from the end, so a wave starts on the
       // k-slices the previous wave loaded last, while L2 still holds them.
@@ -543,7 +561,8 @@ __device__ __forceinline__ void mma_role(const Params& p, uint32_t sbase, uint32
   Unit w;
   for (; next_unit(p, cluster, clusters, i, w); ++i) {
     const uint32_t b = i & 1, aph = (i >> 1) & 1;
-    const uint32_t idesc = w.width == BN ? C::IDESC : C::IDESC_HALF;
+    const uint32_t idesc =
+        w.width == BN ? C::IDESC : (w.width == BN / 2 ? C::IDESC_HALF : C::IDESC_QUARTER);
     if (!wait_spin<true>(bar(BAR_ACC_EMPTY + b), aph ^ 1, wd)) goto done;
     tc_fence_after_sync();   // epilogue's TMEM reads of buffer b precede these MMAs
     {
@@ -637,7 +656,7 @@ __device__ __forceinline__ void epilogue_wide(const Params& p, uint32_t sbase, u
     const int l = w.l;
     const int row_tile = w.mb * C::CS + static_cast<int>(rank);
     const int m0 = row_tile * BM + 32 * q, n0 = w.n0;
-    const int nwide = staging_in_part(p, row_tile, w) * (STAGING / (2 * EPI_N));   // 0, 2 or 4
+    const int nwide = subtiles_in_part(p, row_tile, w) / 2;   // 64-column blocks: 0, 1, 2 or 4
     const uint32_t b = i & 1, aph = (i >> 1) & 1;
     const bool has_acc = w.kb1 > w.kb0;
     auto release_acc = [&]() {
@@ -657,7 +676,7 @@ __device__ __forceinline__ void epilogue_wide(const Params& p, uint32_t sbase, u
       p.trace[(static_cast<size_t>(w.id) * C::CS + rank) * 2] = global_timer_ns();
 #endif
     const uint32_t tacc = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + b * BN;
-    if (nwide == 0) release_acc();   // this CTA's rows lie outside M x N
+    if (hf >= nwide) release_acc();   // no block of this part for this warp
     for (int jw = hf; jw < nwide; jw += 2) {
       uint32_t a0[32], a1[32];
       if (has_acc) {
@@ -727,7 +746,7 @@ __device__ __forceinline__ void epilogue_role(const Params& p, uint32_t sbase, u
     const int l = w.l;
     const int row_tile = w.mb * C::CS + static_cast<int>(rank);   // this CTA's 128-row slab
     const int m0 = row_tile * BM + 32 * q, n0 = w.n0;
-    const int nsub = staging_in_part(p, row_tile, w) * SUB_PER_STAGING;   // 0, 4 or 8
+    const int nsub = subtiles_in_part(p, row_tile, w);   // 0, 2, 4 or 8
     const uint32_t b = i & 1, aph = (i >> 1) & 1;
     const bool has_acc = w.kb1 > w.kb0;   // an MMA ran (K > 0)
 
@@ -1126,7 +1145,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_ws_kernel(const __grid_co
     if (p.num_kb > 0) {
       prefetch_tensormap(&p.tmA);
       prefetch_tensormap(&p.tmB);
-      if (p.num_full < p.num_tiles) prefetch_tensormap(&p.tmB2);
+      if (p.num_full < p.num_tiles) prefetch_tensormap(p.split == 4 ? &p.tmB4 : &p.tmB2);
     }
     if (p.has_c) prefetch_tensormap(&p.tmC);
     prefetch_tensormap(&p.tmD);

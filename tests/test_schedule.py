@@ -4,7 +4,7 @@ The debug library runs the kernel's own unit iterator on the host
 (gemm_ws_debug_schedule) for a given device shape. These tests check, for
 many problem shapes, device shapes and stream-K settings, that
 
-- every ring stage of every output tile (both 128-column halves) is computed
+- every ring stage of every output tile (each 64-column quarter) is computed
   by exactly one unit: nothing is skipped, nothing is done twice;
 - the pieces of a stream-K tile are numbered 0..n-1 by consecutive clusters,
   in K order, and all agree on n and on the first cluster;
@@ -83,14 +83,16 @@ def check(plan, rows, dev, M, N, K, L):
         assert 0 <= key[0] < tm and 0 <= key[1] < tn and 0 <= key[2] < L
     assert sorted(where) == list(range(T)) and len(set(where.values())) == T
 
-    # every stage of every half tile exactly once
-    cover = np.zeros((T, 2, max(ns, 1)), dtype=np.int32)
-    seen_empty = np.zeros((T, 2), dtype=np.int32)
+    # every stage of every 64-column quarter of every tile exactly once
+    cover = np.zeros((T, 4, max(ns, 1)), dtype=np.int32)
+    seen_empty = np.zeros((T, 4), dtype=np.int32)
     for t, n0, width, kb0, kb1 in zip(R["tile"], R["n0"], R["width"], R["kb0"], R["kb1"]):
-        assert width in (BN, BN // 2)
-        halves = [0, 1] if width == BN else [(int(n0) % BN) // (BN // 2)]
+        assert width in (BN, BN // 2, BN // 4)
+        assert int(n0) % width == 0
+        first = (int(n0) % BN) // (BN // 4)
+        quarters = range(first, first + int(width) // (BN // 4))
         assert 0 <= kb0 <= kb1 <= ns
-        for h in halves:
+        for h in quarters:
             if ns == 0:
                 seen_empty[t, h] += 1
             cover[t, h, kb0:kb1] += 1
@@ -238,10 +240,18 @@ def _model_best_halves(T, P, half_cost=0.8):
 def test_half_units_are_the_last_tiles(lib, dev):
     """Half-width units come only from the last tiles in raster order, their
     number matches the stated cost model, and a tile count that is a
-    multiple of the clusters gets none."""
+    multiple of the clusters gets none; problems with at most a quarter as
+    many tiles as clusters run every tile as four quarter units instead."""
     for (M, N, K, L) in SHAPES + [(8192, 8192, 8192, 1), (76 * 512, 256, 4096, 1)]:
         plan, rows = schedule(lib, dev, 0, M, N, K, L)
         T, P = plan[3], dev[2]
+        if 4 * T <= P:
+            # so few tiles that four units per tile fit at once: every tile
+            # runs as four 64-column quarters, one per cluster
+            assert np.all(rows[:, 6] == BN // 4) and len(rows) == 4 * T, (M, N, K, L)
+            assert plan[1] == 4 * T
+            continue
+        assert not np.any(rows[:, 6] == BN // 4)
         halves = sorted({int(t) for t, wd in zip(rows[:, 3], rows[:, 6]) if wd == BN // 2})
         assert halves == list(range(T - len(halves), T)), (M, N, K, L)
         assert len(halves) == _model_best_halves(T, P), (M, N, K, L)
