@@ -41,7 +41,6 @@ struct gemm_ws {
   int k_snake;                    // every other unit of a cluster walks K backwards
   uint32_t* work;                 // [0] stream-out counter, [1] status, [2] done count
   float* partial;                 // stream-K partials: num_sms parts of 128 x 256 fp32
-  uint32_t* split_count;          // stream-K counters, 16 words per SM (kept at zero)
   int last_cuda_error;
   unsigned long long timeout_ns;
   PFN_cuTensorMapEncodeTiled_v12000 encode;
@@ -212,12 +211,11 @@ int64_t cluster_capacity(const gemm_ws* h, int cs) {
 // order) have their K ranges cut into S equal pieces, each run by its own
 // cluster as that cluster's last unit; pieces with the same index sit at the
 // same k on every tile, so concurrent tiles still share A and B panels
-// through L2. The 32 x 32 chunks of a tile are owned round-robin by its
-// pieces; the other pieces park fp32 partials of a chunk in the workspace
-// and the owner adds them to its own accumulator, waiting (bounded) until
-// they are there. Because every piece is its cluster's last unit, nothing a
-// piece waits for can itself be waiting: the waits end as soon as all
-// clusters of the launch are resident.
+// through L2. Every piece writes its fp32 partial of the tile to its own
+// workspace part and waits for nothing; a reduction kernel that follows the
+// GEMM on the stream adds the pieces in piece order and runs the epilogue
+// for those tiles (the separate-reduction variant of the SM90 cooperative
+// kernel's fix-up), so the GEMM needs no co-resident clusters.
 //  - Few tiles (at most half as many as clusters): every tile, S =
 //    min(clusters / tiles, K / kMinShareK, kMaxSplit) (split-K).
 //  - Otherwise the tiles of the last, partial wave if it is at most half
@@ -230,7 +228,7 @@ int64_t cluster_capacity(const gemm_ws* h, int cs) {
 // wherever the shape allows, with pieces down to one ring stage (tests).
 constexpr int64_t kMinShareK = 1024;
 constexpr int64_t kMaxSplit = 16;
-constexpr int64_t kMaxSplitForced = 32;   // owner masks in the kernel hold 32 pieces
+constexpr int64_t kMaxSplitForced = 32;
 // Fix-up of a split tile, measured on GB300 (accumulator complete -> last D
 // store): 7-9 us against ~2 us for a whole tile's epilogue (a chain of L2
 // round trips: partial write, release, count, staged partial reads), plus
@@ -240,8 +238,7 @@ constexpr int64_t kMaxSplitForced = 32;   // owner masks in the kernel hold 32 p
 constexpr double kPieceCostStages = 20.0;
 constexpr size_t kPartBytes = size_t{gws::BM} * gws::BN * sizeof(float);
 // Workspace: one partial part per CTA of a launch (each runs at most one
-// piece), and per CTA of a split tile 8 epilogue-warp counter pairs.
-constexpr size_t kCounterWordsPerSm = 2 * gws::NUM_EPI_WARPS;
+// piece).
 #ifdef GEMM_WS_DEBUG
 constexpr int kScheduleCols = 15;   // columns of a gemm_ws_debug_schedule row
 #endif
@@ -398,7 +395,6 @@ int launch(gemm_ws* h, const uint16_t* A, const uint16_t* B, const uint16_t* C, 
   p.sk_first = static_cast<int>(q.sk_first);
   p.sk_split = static_cast<int>(q.sk_split);
   p.partial = h->partial;
-  p.split_count = h->split_count;
   p.group_m = h->group_m;
   p.k_snake = h->k_snake;
   p.staging_tiles_m = static_cast<int>((M + gws::STAGING - 1) / gws::STAGING);
@@ -454,6 +450,41 @@ int launch(gemm_ws* h, const uint16_t* A, const uint16_t* B, const uint16_t* C, 
     }
   }
   if (e != cudaSuccess) return cuda_fail(h, e);
+  if (q.sk_first < q.num_tiles) {
+    // The split tiles' pieces left fp32 partials; the reduction kernel adds
+    // them and writes those tiles' D, next on the same stream.
+    gws::ReduceParams rp;
+    std::memset(&rp, 0, sizeof rp);
+    rp.partial = h->partial;
+    rp.C = beta != 0.0f ? C : nullptr;
+    rp.D = D;
+    rp.M = p.M;
+    rp.N = p.N;
+    rp.tiles_m = p.tiles_m;
+    rp.tiles_n = p.tiles_n;
+    rp.group_m = p.group_m;
+    rp.cs = cs;
+    rp.sk_first = p.sk_first;
+    rp.sk_tiles = static_cast<int>(q.num_tiles - q.sk_first);
+    rp.sk_split = p.sk_split;
+    rp.alpha = alpha;
+    rp.beta = beta;
+    rp.has_c = p.has_c;
+    const int64_t chunks = static_cast<int64_t>(rp.sk_tiles) * cs * 4 * gws::SUB_PER_PART;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    cfg.gridDim = dim3(static_cast<unsigned>(chunks), 1, 1);   // one block per 32 x 32 chunk
+    cfg.blockDim = dim3(gws::REDUCE_THREADS, 1, 1);
+    cfg.stream = stream;
+    if (h->pdl) {
+      attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+      attr[0].val.programmaticStreamSerializationAllowed = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+    }
+    e = cudaLaunchKernelEx(&cfg, gws::gemm_ws_reduce_kernel, rp);
+    if (e != cudaSuccess) return cuda_fail(h, e);
+  }
   return GEMM_WS_OK;
 }
 
@@ -567,17 +598,13 @@ int gemm_ws_create(gemm_ws_t** out, int device) {
   if (e == cudaSuccess && h->max_pair_clusters < 1) h->cta_group = 1;
   if (e == cudaSuccess) e = cudaMalloc(&h->work, kWorkWords * sizeof(uint32_t));
   if (e == cudaSuccess) e = cudaMemset(h->work, 0, kWorkWords * sizeof(uint32_t));
-  // Stream-K workspace (see kCounterWordsPerSm).
-  const size_t counter_bytes = h->num_sms * kCounterWordsPerSm * 4;
+  // Stream-K workspace: one 128 x 256 fp32 partial per SM.
   if (e == cudaSuccess)
     e = cudaMalloc(&h->partial, static_cast<size_t>(h->num_sms) * kPartBytes);
-  if (e == cudaSuccess) e = cudaMalloc(&h->split_count, counter_bytes);
-  if (e == cudaSuccess) e = cudaMemset(h->split_count, 0, counter_bytes);
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
   if (e != cudaSuccess) {
     if (h->work) cudaFree(h->work);
     if (h->partial) cudaFree(h->partial);
-    if (h->split_count) cudaFree(h->split_count);
     std::free(h);
     return GEMM_WS_ERR_CUDA;
   }
@@ -591,7 +618,6 @@ int gemm_ws_destroy(gemm_ws_t* h) {
   cudaDeviceSynchronize();
   cudaFree(h->work);
   cudaFree(h->partial);
-  cudaFree(h->split_count);
   std::free(h);
   return GEMM_WS_OK;
 }
@@ -641,14 +667,11 @@ int gemm_ws_query_status(gemm_ws_t* h, void* stream) {
   e = cudaMemcpy(&st, h->work + 1, sizeof st, cudaMemcpyDeviceToHost);
   if (e != cudaSuccess) return cuda_fail(h, e);
   if (st != 0) {
-    // An aborted launch may leave split-K counters and the stream-out
-    // counter part-way: start the next launch from zero. The clears go on
-    // `s` and are waited for, so they are complete before this returns
-    // whatever stream the next run uses.
+    // Clear the status word, and the stream-out counters in case an aborted
+    // launch left them part-way, so the next launch starts from zero. The
+    // clear goes on `s` and is waited for, so it is complete before this
+    // returns whatever stream the next run uses.
     e = cudaMemsetAsync(h->work, 0, kWorkWords * sizeof(uint32_t), s);
-    if (e == cudaSuccess)
-      e = cudaMemsetAsync(h->split_count, 0,
-                          static_cast<size_t>(h->num_sms) * kCounterWordsPerSm * 4, s);
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
     if (e != cudaSuccess) return cuda_fail(h, e);
   }
@@ -671,7 +694,7 @@ const char* gemm_ws_status_string(int status) {
 
 #ifdef GEMM_WS_DEBUG
 int gemm_ws_debug_configure(gemm_ws_t* h, int fault, unsigned long long* trace) {
-  if (!h || fault < 0 || fault > 2) return GEMM_WS_ERR_INVALID_ARG;
+  if (!h || fault < 0 || fault > 1) return GEMM_WS_ERR_INVALID_ARG;
   h->debug_fault = fault;
   h->trace = trace;
   return GEMM_WS_OK;

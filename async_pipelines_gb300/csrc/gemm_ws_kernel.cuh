@@ -77,10 +77,8 @@ constexpr int EPI_HALF_WARPS = 4;        // one per lane quarter: a half covers 
 constexpr int STAGING = 128;             // stream-out tile edge
 constexpr int SUB_PER_STAGING = STAGING / EPI_N;
 constexpr int SUB_PER_PART = BN / EPI_N;   // subtiles (32 x 32 chunks per lane quarter) of a part
-constexpr int CHUNK_BYTES = 32 * EPI_N * 4;  // one 32 x 32 fp32 partial chunk
-constexpr int RED_BATCH = 6;                 // partial chunks staged at once per epilogue warp
-constexpr uint32_t RED_AREA_BYTES = RED_BATCH * CHUNK_BYTES;
-static_assert(SUB_PER_PART == 8, "split-K chunk rotation assumes four subtiles per epilogue warp");
+constexpr int CHUNK_FLOATS = 32 * EPI_N;      // one 32 x 32 fp32 partial chunk
+constexpr int PART_FLOATS = 4 * SUB_PER_PART * CHUNK_FLOATS;   // a CTA's 128 x 256 partial
 constexpr int WARP_TMA = 0;
 constexpr int WARP_MMA = 1;
 constexpr int WARP_EPI0 = 2;
@@ -143,8 +141,6 @@ struct Cfg {
   static constexpr uint32_t IDESC_HALF = idesc_bf16_f32(TILE_M, BN / 2);
   static constexpr uint32_t IDESC_QUARTER = idesc_bf16_f32(TILE_M, BN / 4);
   static_assert(STAGES <= NUM_STAGES_MAX, "barrier table");
-  static_assert(OFF_B + STAGES * B_STAGE_BYTES - OFF_A >= NUM_EPI_WARPS * RED_AREA_BYTES,
-                "the split-K reduction stages partials in the operand ring");
   static_assert(SMEM_BYTES <= 232448, "exceeds the 227 KiB per-CTA shared memory");
   static_assert(OFF_B % 1024 == 0 && OFF_D % 1024 == 0 && OFF_C % 1024 == 0, "alignment");
 };
@@ -169,8 +165,6 @@ struct Params {
   int sk_first;
   int sk_split;
   float* partial;                // piece partials: [cluster][CTA][chunk] x 1024 fp32
-  uint32_t* split_count;         // [stream-K tile][CTA][epilogue warp] {pieces counted in,
-                                 // owners done}, returned to 0 by the last owner
   int group_m;                   // raster: tiles walk group_m m-tiles per n step
   int k_snake;                   // 1: every other unit of a cluster walks K backwards
   int staging_tiles_m;           // ceil(M / 128)
@@ -196,17 +190,22 @@ struct Params {
 // Tile t -> (m block, n block, batch). Within a batch, tiles go down a group
 // of `group_m` m-blocks, then step n, so the CTAs resident at one time share
 // their A rows and B columns through L2.
-__host__ __device__ __forceinline__ void tile_coords(const Params& p, int t, int& mb, int& nb, int& l) {
-  const int per_batch = p.tiles_m * p.tiles_n;
+__host__ __device__ __forceinline__ void tile_coords_of(int tiles_m, int tiles_n, int group_m,
+                                                        int t, int& mb, int& nb, int& l) {
+  const int per_batch = tiles_m * tiles_n;
   l = t / per_batch;
   const int r = t - l * per_batch;
-  const int group_tiles = p.group_m * p.tiles_n;
+  const int group_tiles = group_m * tiles_n;
   const int g = r / group_tiles;
-  const int first_m = g * p.group_m;
-  const int gm = p.tiles_m - first_m < p.group_m ? p.tiles_m - first_m : p.group_m;
+  const int first_m = g * group_m;
+  const int gm = tiles_m - first_m < group_m ? tiles_m - first_m : group_m;
   const int rr = r - g * group_tiles;
   mb = first_m + rr % gm;
   nb = rr / gm;
+}
+
+__host__ __device__ __forceinline__ void tile_coords(const Params& p, int t, int& mb, int& nb, int& l) {
+  tile_coords_of(p.tiles_m, p.tiles_n, p.group_m, t, mb, nb, l);
 }
 
 // A unit of work: a tile (256 columns, or, for the last tiles in raster
@@ -401,23 +400,6 @@ template <bool kCluster>
 __device__ __forceinline__ bool wait_spin(uint32_t bar, uint32_t parity, const Watchdog& wd) {
   if (kCluster ? mbar_test_wait_cluster(bar, parity) : mbar_test_wait(bar, parity)) return true;
   return spin_slow<kCluster>(bar, parity, wd);
-}
-
-// Bounded wait (one thread) until a global counter reaches `target`, with
-// acquire semantics. Returns false if the CTA is aborting or the wait
-// exceeded the limit (which then starts the abort).
-__device__ __noinline__ bool wait_count(const uint32_t* cnt, uint32_t target, const Watchdog& wd) {
-  if (ld_acquire_gpu(cnt) >= target) return true;
-  const uint64_t t0 = global_timer_ns();
-  for (;;) {
-    if (ld_acquire_gpu(cnt) >= target) return true;
-    if (*wd.abort) return false;
-    if (global_timer_ns() - t0 > wd.limit_ns) {
-      *wd.abort = 1;
-      atomicExch(wd.status, STATUS_TIMEOUT);
-      return false;
-    }
-  }
 }
 
 // Short bounded wait used only while draining after an abort.
@@ -861,156 +843,33 @@ __device__ __forceinline__ void epilogue_role(const Params& p, uint32_t sbase, u
       }
     } else {
       // A piece of the tile's K range (every piece of a tile runs on its own
-      // cluster, as that cluster's last unit). Each of the warp's four 32 x 32
-      // chunks (TMEM lane quarter q, subtiles j = hf + 2k) has an owner piece;
-      // the others park their fp32 partial of it in the workspace (TMEM
-      // register order: float4 c of lane r at [c][r], so a warp's store or
-      // load is 512 contiguous bytes) and count in on the warp's chunk-group
-      // counter with a release add. The owner waits (bounded) for all pieces
-      // to count in, adds the partials to its own accumulator in piece order
-      // (so the bits do not depend on which piece owns the chunk) and runs
-      // the epilogue for the chunk: the fixup / compute_epilogue step of the
-      // SM90 cooperative kernel. Owners are spread round-robin over the
-      // pieces, so the reduction is shared by all of them.
-      const int S = w.pieces;
-      auto chunk_of = [&](int piece, int j) -> float* {
-        const size_t part = static_cast<size_t>(sk_slot(p, w, piece)) * C::CS + rank;
-        return p.partial + ((part * 4 + q) * SUB_PER_PART + j) * (32 * EPI_N);
-      };
-      auto owner = [&](int k) { return (e * (SUB_PER_PART / 2) + k) % S; };
-      uint32_t* cnt = p.split_count + ((static_cast<size_t>(w.sk_tile) * C::CS + rank) *
-                                           NUM_EPI_WARPS + e) * 2;
-      uint32_t own = 0;      // bit k: this piece owns chunk k (inside N)
-      uint32_t owners = 0;   // bit o: piece o owns a chunk of this warp (o < 32)
-      int valid = 0;
-      for (int k = 0; k < SUB_PER_PART / 2; ++k) {
-        if (hf + 2 * k >= nsub) continue;   // outside N (or this CTA's rows outside M)
-        ++valid;
-        owners |= 1u << (owner(k) & 31);
-        if (owner(k) == w.piece) own |= 1u << k;
-      }
-      // 1) The partials of the chunks other pieces own.
+      // cluster, as that cluster's last unit): this warp's fp32 partial of
+      // each of its 32 x 32 chunks (TMEM lane quarter q, subtiles j = hf +
+      // 2k) goes to the piece's workspace part, in TMEM register order
+      // (float4 c of lane r at [c][r], so a warp's store is 512 contiguous
+      // bytes). Nothing here waits for another piece: the reduction kernel
+      // that follows on the stream adds the pieces and runs the epilogue (the
+      // separate-reduction variant of the SM90 cooperative kernel's fix-up).
+      float* part = p.partial + (static_cast<size_t>(sk_slot(p, w, w.piece)) * C::CS + rank) *
+                                    PART_FLOATS;
+#pragma unroll 1
       for (int k = 0; k < SUB_PER_PART / 2; ++k) {
         const int j = hf + 2 * k;
-        if (j >= nsub || (own >> k) & 1u) continue;
+        if (j >= nsub) break;   // outside N (or this CTA's rows outside M)
         uint32_t acc[32];
         tmem_ld_32x32b_x32(tacc + j * EPI_N, acc);
         tmem_wait_ld();
-        float4* dst = reinterpret_cast<float4*>(chunk_of(w.piece, j));
+        float4* dst = reinterpret_cast<float4*>(part + (q * SUB_PER_PART + j) * CHUNK_FLOATS);
 #pragma unroll
         for (int c = 0; c < 8; ++c)
           __stcg(dst + c * 32 + lane,
                  make_float4(__uint_as_float(acc[4 * c]), __uint_as_float(acc[4 * c + 1]),
                              __uint_as_float(acc[4 * c + 2]), __uint_as_float(acc[4 * c + 3])));
       }
+      release_acc();
 #ifdef GEMM_WS_DEBUG
       if (p.phases && e == 0 && lane == 0) p.phases[blockIdx.x * 8 + 3] = global_timer_ns();
 #endif
-      if (valid > 0) {
-        fence_acq_rel_gpu();   // this lane's partials before the count (the warp syncs below)
-        __syncwarp();
-#ifdef GEMM_WS_DEBUG
-        // injected fault 2: piece 1 never counts in, so owners can only stop
-        // waiting through the watchdog
-        if (lane == 0 && !(p.debug_fault == 2 && w.piece == 1)) red_release_gpu_add(cnt, 1u);
-#else
-        if (lane == 0) red_release_gpu_add(cnt, 1u);
-#endif
-      }
-#ifdef GEMM_WS_DEBUG
-      if (p.phases && e == 0 && lane == 0) p.phases[blockIdx.x * 8 + 4] = global_timer_ns();
-#endif
-      if (own == 0) {
-        release_acc();
-      } else {
-        // 2) Every piece has counted in: its partials of this warp's chunks are there.
-        uint32_t in = 0;
-        if (lane == 0) in = wait_count(cnt, static_cast<uint32_t>(S), wd) ? 1u : 0u;
-        in = __shfl_sync(0xffffffffu, in, 0);
-        if (!in) {
-          release_acc();
-          break;
-        }
-        fence_acq_rel_gpu();   // acquire, for every lane, the partials counted in
-#ifdef GEMM_WS_DEBUG
-        if (p.phases && e == 0 && lane == 0) p.phases[blockIdx.x * 8 + 5] = global_timer_ns();
-#endif
-
-        // 3) The owned chunks: own accumulator plus the other pieces' partials.
-        const uint32_t area = sbase + C::OFF_A + static_cast<uint32_t>(e) * RED_AREA_BYTES;
-        int k = __ffs(own) - 1;
-        if (p.has_c) issue_c(hf + 2 * k);
-        while (k >= 0) {
-          const int j = hf + 2 * k;
-          const uint32_t rest = own & ~((2u << k) - 1u);
-          const int next = rest ? __ffs(rest) - 1 : -1;
-          float v[32];
-#pragma unroll
-          for (int x = 0; x < 32; ++x) v[x] = 0.0f;
-          // Sum in piece order, this piece's own part straight from TMEM at
-          // its place. The other pieces' partials come in batches of up to
-          // RED_BATCH through the warp's share of the operand ring (idle: this
-          // is the cluster's last unit and its MMAs are done): every lane
-          // copies its own 16-byte pieces with cp.async, a batch in flight at
-          // once, then reads back only what it copied. (One batch for all
-          // pieces, in a larger share of the ring, measured slower.)
-          for (int pc = 0; pc < S;) {
-            int n = 0, end = pc;
-            for (; end < S && n < RED_BATCH; ++end)
-              if (end != w.piece) ++n;
-            int b2 = 0;
-            for (int pb = pc; pb < end; ++pb) {
-              if (pb == w.piece) continue;
-              const float4* src = reinterpret_cast<const float4*>(chunk_of(pb, j)) + lane;
-#pragma unroll
-              for (int c = 0; c < 8; ++c)
-                cp_async_16(area + b2 * CHUNK_BYTES + (c * 32 + lane) * 16, src + c * 32);
-              ++b2;
-            }
-            cp_async_wait_all();
-            for (b2 = 0; pc < end; ++pc) {
-              if (pc == w.piece) {
-                uint32_t acc[32];
-                tmem_ld_32x32b_x32(tacc + j * EPI_N, acc);
-                tmem_wait_ld();
-#pragma unroll
-                for (int x = 0; x < 32; ++x) v[x] += __uint_as_float(acc[x]);
-                continue;
-              }
-              const float4* sp4 =
-                  reinterpret_cast<const float4*>(smem + (area - sbase) + b2 * CHUNK_BYTES) + lane;
-#pragma unroll
-              for (int c = 0; c < 8; ++c) {
-                const float4 f = sp4[c * 32];
-                v[4 * c] += f.x;
-                v[4 * c + 1] += f.y;
-                v[4 * c + 2] += f.z;
-                v[4 * c + 3] += f.w;
-              }
-              ++b2;
-            }
-          }
-          if (next < 0) release_acc();   // every TMEM read of this unit is done
-#pragma unroll
-          for (int x = 0; x < 32; ++x) v[x] *= p.alpha;
-          if (!finish_subtile(j, v, next >= 0 ? hf + 2 * next : -1)) {
-            ok = false;
-            break;
-          }
-          k = next;
-        }
-#ifdef GEMM_WS_DEBUG
-        if (p.phases && e == 0 && lane == 0) p.phases[blockIdx.x * 8 + 6] = global_timer_ns();
-#endif
-        // 4) The last owner to finish returns the warp's counters to zero.
-        if (ok && lane == 0) {
-          const uint32_t n_owners = static_cast<uint32_t>(__popc(owners));
-          if (atomicAdd(cnt + 1, 1u) == n_owners - 1) {
-            atomicExch(cnt, 0u);
-            atomicExch(cnt + 1, 0u);
-          }
-        }
-      }
     }
     if (!ok) break;
 #ifdef GEMM_WS_DEBUG
@@ -1211,6 +1070,105 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_ws_kernel(const __grid_co
 #ifdef GEMM_WS_DEBUG
   if (p.phases && threadIdx.x == 0) p.phases[blockIdx.x * 8 + 2] = global_timer_ns();
 #endif
+}
+
+// ------------------------------------------------------------ split reduction
+
+// The pieces of the split tiles, combined: one warp per 32 x 32 chunk of a
+// split tile's CTA part adds the chunk's fp32 partials of all S pieces in
+// piece order, then forms alpha * sum + beta * C, rounds it to bf16 and
+// stores D. It runs as its own kernel after the GEMM on the same stream (the
+// separate-reduction variant of the SM90 cooperative kernel's fix-up), so no
+// piece ever waits for another and the GEMM needs no co-resident clusters.
+struct ReduceParams {
+  const float* partial;   // the GEMM's piece partials (see Params::partial)
+  const uint16_t* C;      // L x M x N bf16, read iff has_c (may be D itself)
+  uint16_t* D;            // L x M x N bf16
+  int M, N;
+  int tiles_m, tiles_n, group_m;   // the GEMM launch's tile grid and raster
+  int cs;                          // CTAs per cluster: a tile has 128 * cs rows
+  int sk_first, sk_tiles, sk_split;
+  float alpha, beta;
+  int has_c;
+};
+
+constexpr int REDUCE_THREADS = 256;   // one thread per float4 of a 32 x 32 chunk
+constexpr int REDUCE_INFLIGHT = 8;    // pieces whose loads a thread keeps in flight
+
+// One block per chunk. Thread t holds float4 c = t / 32 of chunk row r = t %
+// 32 (the workspace layout, so the 256 threads read 4 KiB contiguously per
+// piece), loads REDUCE_INFLIGHT pieces at a time and adds them in piece
+// order; the sums then pass through shared memory so that C and D are read
+// and written along rows.
+__global__ void __launch_bounds__(REDUCE_THREADS)
+    gemm_ws_reduce_kernel(const __grid_constant__ ReduceParams p) {
+  __shared__ float sum[32][EPI_N + 4];   // padded rows: conflict-free both ways
+  // The GEMM grid before this one in the stream has written every partial.
+  grid_dependency_wait();
+  if (threadIdx.x == 0) grid_launch_dependents();
+  const int x = blockIdx.x;                          // chunk
+  const int per_part = 4 * SUB_PER_PART;             // chunks of one CTA's 128 x 256 part
+  const int per_tile = p.cs * per_part;
+  const int r = x / per_tile;
+  const int rank = (x - r * per_tile) / per_part;
+  const int cq = x - r * per_tile - rank * per_part;
+  const int q = cq / SUB_PER_PART, j = cq - q * SUB_PER_PART;
+  int mb, nb, l;
+  tile_coords_of(p.tiles_m, p.tiles_n, p.group_m, p.sk_first + r, mb, nb, l);
+  const int row_tile = mb * p.cs + rank;
+  const int col0 = nb * BN + j * EPI_N;
+  // Chunks outside M x N were not written by the pieces and hold no output.
+  if (row_tile * BM >= p.M || col0 >= p.N) return;   // block-uniform
+  const int t = threadIdx.x;
+  const float4* src = reinterpret_cast<const float4*>(
+                          p.partial + (static_cast<size_t>(r) * p.sk_split * p.cs + rank) *
+                                          PART_FLOATS +
+                          (q * SUB_PER_PART + j) * CHUNK_FLOATS) +
+                      t;
+  const size_t piece_stride = static_cast<size_t>(p.cs) * PART_FLOATS / 4;   // float4s
+  float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+  for (int s0 = 0; s0 < p.sk_split; s0 += REDUCE_INFLIGHT) {
+    float4 f[REDUCE_INFLIGHT];
+#pragma unroll
+    for (int k = 0; k < REDUCE_INFLIGHT; ++k)
+      if (s0 + k < p.sk_split) f[k] = __ldcg(src + (s0 + k) * piece_stride);
+#pragma unroll
+    for (int k = 0; k < REDUCE_INFLIGHT; ++k) {
+      if (s0 + k < p.sk_split) {
+        acc.x += f[k].x;
+        acc.y += f[k].y;
+        acc.z += f[k].z;
+        acc.w += f[k].w;
+      }
+    }
+  }
+  {
+    const int cr = t % 32, c4 = t / 32;   // chunk row, float4 column
+    sum[cr][4 * c4] = acc.x;
+    sum[cr][4 * c4 + 1] = acc.y;
+    sum[cr][4 * c4 + 2] = acc.z;
+    sum[cr][4 * c4 + 3] = acc.w;
+  }
+  __syncthreads();
+  // Row-wise epilogue: thread t takes 4 columns of chunk row t / 8.
+  const int cr = t / 8, c0 = 4 * (t % 8);
+  const int row = row_tile * BM + 32 * q + cr;
+  if (row >= p.M || col0 + c0 >= p.N) return;        // N is a multiple of 8
+  const size_t at = (static_cast<size_t>(l) * p.M + row) * p.N + col0 + c0;
+  float o[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) o[k] = sum[cr][c0 + k] * p.alpha;
+  if (p.has_c) {
+    const uint2 raw = *reinterpret_cast<const uint2*>(p.C + at);
+    o[0] = fmaf(p.beta, __uint_as_float(raw.x << 16), o[0]);
+    o[1] = fmaf(p.beta, __uint_as_float(raw.x & 0xFFFF0000u), o[1]);
+    o[2] = fmaf(p.beta, __uint_as_float(raw.y << 16), o[2]);
+    o[3] = fmaf(p.beta, __uint_as_float(raw.y & 0xFFFF0000u), o[3]);
+  }
+  uint2 out;
+  out.x = pack_bf16x2(o[0], o[1]);
+  out.y = pack_bf16x2(o[2], o[3]);
+  *reinterpret_cast<uint2*>(p.D + at) = out;
 }
 
 }  // namespace gws

@@ -27,7 +27,7 @@
  * device; the caller owns it and keeps it alive until the stream work ends.
  * The handle owns only its device workspace: the stream-out sequence
  * counter, a status word, a completion count, and the split-K area (one
- * 128 x 256 fp32 partial and 16 counter words per SM, ~128 KiB per SM).
+ * 128 x 256 fp32 partial per SM, 128 KiB per SM).
  * The kernel returns every counter to zero before it ends, so runs need no
  * clearing between them; runs on one handle that overlap on the GPU (e.g. on
  * two streams) race on that workspace: serialise them or use one handle per
@@ -97,9 +97,10 @@ int gemm_ws_destroy(gemm_ws_t* h);
  * tiles is at most half full, those tiles' K ranges may be cut into 2..16
  * equal pieces of >= 1024 that run on separate clusters (chosen by a host
  * cost model); acc is then the sum, in piece order, of the pieces' fp32
- * partials (deterministic: the same bits on every run). The pieces of a tile
- * wait for each other (bounded by the watchdog), which needs every cluster
- * of the launch resident at once, as on a whole, unshared GPU.
+ * partials (deterministic: the same bits on every run). The pieces write
+ * their partials and wait for nothing; a second, small kernel that the call
+ * launches after the GEMM on the same stream adds them and writes those
+ * tiles' D, so the call works on a GPU shared with other kernels too.
  * GEMM_WS_STREAM_K in the environment at gemm_ws_create sets this per
  * handle: 0 off, 1 (default) by the cost model, 2 wherever the shape allows
  * (pieces down to one ring stage). gemm_ws_run_streamout never splits.

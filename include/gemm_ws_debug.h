@@ -26,10 +26,7 @@ extern "C" {
 
 /* Sets the handle's debug state for its later runs.
  *  - fault: 0 none; 1 the stream-out consumer warp returns at once, so the
- *    epilogue's wait for a free slot can only end by the watchdog; 2 piece 1
- *    of every split tile never counts its partials in, so the owners' waits
- *    for all pieces can only end by the watchdog (and leave the tile's
- *    counters part-way, for gemm_ws_query_status to clear).
+ *    epilogue's wait for a free slot can only end by the watchdog.
  *  - trace: device buffer of num_units * ctas_per_cluster * 2 uint64 (see
  *    gemm_ws_debug_launch_shape) or NULL. For work unit u and CTA rank r
  *    in its cluster, trace[(u*ctas_per_cluster + r)*2] = global time (ns) at which
@@ -46,10 +43,9 @@ int gemm_ws_debug_configure(gemm_ws_t* h, int fault, unsigned long long* trace);
  * handle's later launches (size it with gemm_ws_debug_launch_shape:
  * clusters * ctas_per_cluster CTAs): for CTA b, phases[8b] = global time
  * (ns) at kernel entry, [8b+1] = after the wait for the previous grid in
- * the stream, [8b+2] = at exit; for the CTA's last split piece, as seen by
- * its first epilogue warp: [8b+3] partials written, [8b+4] counted in,
- * [8b+5] all pieces counted in (owners only), [8b+6] owned chunks stored
- * (owners only). Slots not reached stay as the caller left them. The
+ * the stream, [8b+2] = at exit; for the CTA's split piece, as seen by its
+ * first epilogue warp: [8b+3] its partials written to the workspace. Slots
+ * not reached stay as the caller left them. The
  * caller owns the buffer. Returns GEMM_WS_OK or GEMM_WS_ERR_INVALID_ARG. */
 int gemm_ws_debug_phases(gemm_ws_t* h, unsigned long long* phases);
 

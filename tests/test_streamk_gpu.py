@@ -139,9 +139,10 @@ def test_stream_k_integer_inputs_bit_exact(cfg):
         np.testing.assert_array_equal(bits_of(D).reshape(L * M, N)[rows], f64_to_bf16_bits(ref))
 
 
-def test_stream_k_counters_reset_between_launches(cfg):
-    """Different data back to back: a counter left non-zero by one launch
-    would make the wrong piece (or none) finish a chunk in the next."""
+def test_stream_k_workspace_reused_between_launches(cfg):
+    """Different data back to back through the same partial workspace: each
+    launch's reduction must read that launch's partials, never a previous
+    launch's."""
     auto, forced, plan_auto, plan_forced = cfg
     for g, plan, (M, N, K, L) in ((auto, plan_auto, (256, 512, 6144, 1)),
                                   (forced, plan_forced, (1280, 1536, 768, 1))):
@@ -159,7 +160,7 @@ def test_stream_k_counters_reset_between_launches(cfg):
 
 def test_stream_k_is_deterministic(cfg):
     """The pieces are summed in a fixed order: the same bits every launch,
-    whichever piece happened to finish a chunk's count."""
+    whichever piece happened to finish first."""
     auto, forced, plan_auto, plan_forced = cfg
     for g, plan, (M, N, K, L) in ((auto, plan_auto, (512, 512, 16384, 1)),
                                   (forced, plan_forced, (2048, 1024, 1024, 1))):
@@ -229,3 +230,35 @@ def test_plan_keeps_whole_tiles_where_it_should(cfg):
         assert sk_tiles(plan, 1024, 1024, 32768, 1, streamout=True) == 0
         assert sk_tiles(plan, 256, 256, 0, 1) == 0
     assert sk_tiles(plan_auto, 1024, 1024, 1024, 1) == 0
+
+
+def test_split_gemm_beside_kernels_on_another_stream(cfg):
+    """Split pieces never wait for one another, so a split GEMM is correct
+    (and ends with status OK) while other work on another stream holds SMs:
+    cuBLAS GEMMs keep a second stream busy for the whole call (bounded: a
+    fixed number of library calls)."""
+    auto, _, plan, _ = cfg
+    M, N, K, L = 512, 512, 16384, 1
+    assert sk_tiles(plan, M, N, K, L) > 0
+    A, B, C = workloads.make_inputs(M, N, K, L, ("uniform",), ("normal", 1.0), seed=55)
+    Ad, Bd, Cd = A.cuda(), B.cuda(), C.cuda()
+    X = torch.randn(4096, 4096, device="cuda", dtype=torch.bfloat16)
+    Y = torch.empty_like(X)
+    side = torch.cuda.Stream()
+    D = torch.empty(L, M, N, dtype=torch.bfloat16, device="cuda")
+    results = []
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        for _ in range(200):
+            torch.matmul(X, X, out=Y)
+    for _ in range(10):
+        D.fill_(float("nan"))
+        auto.run(Ad, Bd, Cd, D, 1.0, 0.5)
+        results.append(D.clone())
+    torch.cuda.synchronize()
+    assert auto.query_status() == gemm_ws.OK
+    rows = sample_rows(M, L, 32, seed=4)
+    ref = oracle.gemm_rows(bits_of(A), bits_of(B), bits_of(C), M, N, K, L, 1.0, 0.5, rows=rows)
+    for n, R in enumerate(results):
+        assert torch.equal(R.view(torch.int16), results[0].view(torch.int16)), n
+    assert_gemm_close(bits_of(results[0]).reshape(L * M, N)[rows], ref, K, "beside other kernels")
