@@ -229,13 +229,12 @@ int64_t cluster_capacity(const gemm_ws* h, int cs) {
 constexpr int64_t kMinShareK = 1024;
 constexpr int64_t kMaxSplit = 16;
 constexpr int64_t kMaxSplitForced = 32;
-// Fix-up of a split tile, measured on GB300 (accumulator complete -> last D
-// store): 7-9 us against ~2 us for a whole tile's epilogue (a chain of L2
-// round trips: partial write, release, count, staged partial reads), plus
-// the pipeline fill of a short piece; at ~0.5-0.6 us per ring stage, ~20
-// stages. With this cost a split is taken only where it measured faster
-// (e.g. not for 4096^3's or 1536^2 x 8192's tail, where half-width tiles win).
-constexpr double kPieceCostStages = 20.0;
+// Fix-up cost of a split tile, in ring stages of MMA work (~0.5-0.6 us each
+// on GB300): the pieces' partial writes, the reduction kernel after the GEMM
+// and a short piece's pipeline fill. Calibrated by timing: 10 splits
+// 1536^2 x 8192's tail (-1.8 %) and leaves 4096^3's to half-width tiles; 5 or
+// less also split 4096^3's, which then measured 4 % slower.
+constexpr double kPieceCostStages = 10.0;
 constexpr size_t kPartBytes = size_t{gws::BM} * gws::BN * sizeof(float);
 // Workspace: one partial part per CTA of a launch (each runs at most one
 // piece).
@@ -796,6 +795,17 @@ int gemm_ws_debug_schedule(int cta_group, int num_sms, int max_clusters, int str
 int64_t gemm_ws_streamout_tiles(int64_t M, int64_t N, int64_t L) {
   if (M <= 0 || N <= 0 || L <= 0) return 0;
   return L * ((M + gws::STAGING - 1) / gws::STAGING) * ((N + gws::STAGING - 1) / gws::STAGING);
+}
+
+int gemm_ws_kernels_per_run(gemm_ws_t* h, int64_t M, int64_t N, int64_t K, int64_t L,
+                            int streamout) {
+  if (!h) return -GEMM_WS_ERR_INVALID_ARG;
+  if (M < 0 || N < 0 || K < 0 || L < 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim ||
+      L > kMaxDim)
+    return -GEMM_WS_ERR_INVALID_ARG;
+  if (M * N * L == 0) return 0;
+  const Plan q = make_plan(h, M, N, K, L, streamout != 0);
+  return q.sk_first < q.num_tiles ? 2 : 1;
 }
 
 }  // extern "C"

@@ -25,7 +25,7 @@ ERR_TIMEOUT = 5
 EXPORTS = (
     "gemm_ws_create", "gemm_ws_destroy", "gemm_ws_run", "gemm_ws_run_streamout",
     "gemm_ws_query_status", "gemm_ws_last_cuda_error", "gemm_ws_status_string",
-    "gemm_ws_streamout_tiles", "gemm_ws_run_streamout_noalloc",
+    "gemm_ws_streamout_tiles", "gemm_ws_run_streamout_noalloc", "gemm_ws_kernels_per_run",
 )
 
 STAGING_TILE = 128
@@ -72,6 +72,8 @@ def load_library(path: Optional[str] = None):
     lib.gemm_ws_status_string.restype = ctypes.c_char_p
     lib.gemm_ws_streamout_tiles.argtypes = [i64, i64, i64]
     lib.gemm_ws_streamout_tiles.restype = i64
+    lib.gemm_ws_kernels_per_run.argtypes = [vp, i64, i64, i64, i64, ctypes.c_int]
+    lib.gemm_ws_kernels_per_run.restype = ctypes.c_int
     for name in ("gemm_ws_create", "gemm_ws_destroy", "gemm_ws_run", "gemm_ws_run_streamout",
                  "gemm_ws_query_status", "gemm_ws_last_cuda_error",
                  "gemm_ws_run_streamout_noalloc"):
@@ -266,3 +268,10 @@ class GemmWS:
 
     def query_status(self, stream=None) -> int:
         return self.lib.gemm_ws_query_status(self.handle, _stream(stream))
+
+    def kernels_per_run(self, M, N, K, L, streamout=False) -> int:
+        """Kernels one run of this problem launches (1, or 2 with split pieces)."""
+        n = self.lib.gemm_ws_kernels_per_run(self.handle, M, N, K, L, int(bool(streamout)))
+        if n < 0:
+            raise GemmWSError(-n, "gemm_ws_kernels_per_run")
+        return n

@@ -167,6 +167,18 @@ const char* gemm_ws_status_string(int status);
  * gemm_ws_run_streamout. Pure host arithmetic; needs no GPU. */
 int64_t gemm_ws_streamout_tiles(int64_t M, int64_t N, int64_t L);
 
+/* Kernels that a run of this problem on this handle launches on its stream:
+ * 1, or 2 when some tiles are split into K pieces (the GEMM, then the
+ * reduction of the pieces); 0 for an empty problem (M*N*L == 0); negative
+ * (a gemm_ws_status, negated) for invalid sizes or a NULL handle. streamout:
+ * nonzero for gemm_ws_run_streamout, which never splits. Host arithmetic
+ * only, the same plan the run makes; useful for counting launches or sizing
+ * CUDA-graph captures.
+ * Defined by: no page; the SM90 cooperative kernel header's separate-
+ * reduction variant of the stream-K fix-up is what adds the second kernel. */
+int gemm_ws_kernels_per_run(gemm_ws_t* h, int64_t M, int64_t N, int64_t K, int64_t L,
+                            int streamout);
+
 /* gemm_ws_run_streamout for callers that cannot allocate device memory.
  *
  * The cited CUTLASS sources have no counterpart: this is a library

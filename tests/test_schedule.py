@@ -174,8 +174,11 @@ def test_stream_k_where_expected(lib):
     assert sk(256, 256, 8192, 1) == 1
     assert sk(2048, 2048, 16384, 1) == 0       # one partial wave, over half full: whole tiles
     assert sk(4096, 4096, 4096, 1) == 0        # 256 = 3 * 76 + 28: half-width tail is cheaper
-    assert sk(8192, 8192, 8192, 1) == 0        # 1024 = 13 * 76 + 36: no measured gain
-    assert sk(1536, 1536, 8192, 1) == 0        # 36 tiles: half-width tiles measured faster
+    # 1024 = 13 * 76 + 36 and 36 tiles: the last partial wave split in two
+    # pieces per tile (measured ~0.6 us faster than half-width tiles in both)
+    assert sk(8192, 8192, 8192, 1) == 36
+    assert sk(1536, 1536, 8192, 1) == 36
+    assert sk(8192, 8192, 4096, 1) == 0        # 32-stage tiles: half-width tail is cheaper
     assert sk(1024, 1024, 1024, 1) == 0        # short K: pieces would be too small
     assert sk(256, 256, 0, 1) == 0
     # 152 tiles = exactly two waves of 76 clusters: nothing to balance

@@ -262,3 +262,17 @@ def test_split_gemm_beside_kernels_on_another_stream(cfg):
     for n, R in enumerate(results):
         assert torch.equal(R.view(torch.int16), results[0].view(torch.int16)), n
     assert_gemm_close(bits_of(results[0]).reshape(L * M, N)[rows], ref, K, "beside other kernels")
+
+
+def test_kernels_per_run_matches_the_plan(cfg):
+    """The public launch count: 2 exactly where the plan splits tiles into
+    pieces (the GEMM and the reduction), 1 otherwise, 0 for empty problems."""
+    auto, forced, plan_auto, plan_forced = cfg
+    shapes = [(256, 256, 8192, 1), (1024, 1024, 1024, 1), (8192, 8192, 8192, 1),
+              (4096, 4096, 4096, 1), (200, 296, 16384, 3), (4096, 2560, 512, 1)]
+    for g, plan in ((auto, plan_auto), (forced, plan_forced)):
+        for M, N, K, L in shapes:
+            want = 2 if sk_tiles(plan, M, N, K, L) > 0 else 1
+            assert g.kernels_per_run(M, N, K, L) == want, (M, N, K, L)
+            assert g.kernels_per_run(M, N, K, L, streamout=True) == 1
+        assert g.kernels_per_run(0, 64, 64, 1) == 0
