@@ -484,6 +484,12 @@ __device__ __forceinline__ void producer_role(const Params& p, uint32_t sbase, u
       ++g;
       // try-acquire the NEXT stage before this stage's copies go out
       token = mbar_test_wait(empty(g % C::STAGES), ((g / C::STAGES) & 1) ^ 1);
+      if (g == 1) {
+        grid_dependency_wait();   // A and B may be the previous kernel's output
+#ifdef GEMM_WS_DEBUG
+        if (p.phases && threadIdx.x == 0) p.phases[blockIdx.x * 8 + 1] = global_timer_ns();
+#endif
+      }
       if (leader) mbar_arrive_expect_tx(full(s), tx);
       // Both CTAs' copies complete on the pair's even CTA's full[s]. Slabs
       // past K (a ragged last stage) are zero-filled by the TMA.
@@ -632,6 +638,7 @@ __device__ __forceinline__ void epilogue_wide(const Params& p, uint32_t sbase, u
   const int cluster = blockIdx.x / C::CS, clusters = gridDim.x / C::CS;
   uint8_t* dq = smem + C::OFF_D + hf * (4 * WIDE_QUARTER_BYTES) + q * WIDE_QUARTER_BYTES;
   const uint32_t wrow = lane * 128, wswz = lane & 7;
+  grid_dependency_wait();   // D may be read or written by the previous kernel
   int i = 0;
   Unit w;
   for (; next_unit(p, cluster, clusters, i, w); ++i) {
@@ -722,6 +729,7 @@ __device__ __forceinline__ void epilogue_role(const Params& p, uint32_t sbase, u
   uint32_t u = 0;        // subtiles stored by this warp (slot ring position)
   uint32_t cu = 0;       // C subtiles consumed by this warp
   uint32_t c_issued = 0; // C subtile loads issued by this warp
+  grid_dependency_wait();   // C and D may be the previous kernel's output or input
   int i = 0;
   Unit w;
   for (; next_unit(p, cluster, clusters, i, w); ++i) {
@@ -897,6 +905,7 @@ __device__ __forceinline__ void consumer_role(const Params& p, uint32_t sbase, u
   using C = Cfg<CG>;
   auto bar = [&](int i) { return sbase + C::OFF_BAR + 8 * i; };
   const int cluster = blockIdx.x / C::CS, clusters = gridDim.x / C::CS;
+  grid_dependency_wait();   // staging and flags may be in use by the previous kernel
   // Each stream-out tile has exactly one publishing consumer, which clears
   // the tile's flag words before anything else; so no host-side clearing is
   // needed and nothing in this launch can observe a stale ready word.
@@ -1027,17 +1036,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_ws_kernel(const __grid_co
   const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
   const Watchdog wd{abort_flag, p.status, p.timeout_ns};
   // Everything above touches only this CTA's shared and tensor memory, so it
-  // may overlap the previous kernel's tail; global memory is touched only
-  // after that kernel has completed. The next launch may be scheduled now
-  // (its CTAs take SMs as this grid's CTAs leave them).
-  grid_dependency_wait();
+  // may overlap the previous kernel's tail. Global memory is touched only
+  // after that kernel has completed: each role that reads or writes global
+  // memory waits for it (grid_dependency_wait) just before its first such
+  // access, so the rest of its set-up (unit coordinates, first barrier
+  // waits, the first run of its code) overlaps the previous kernel too. The
+  // MMA thread never touches global memory. The next launch may be
+  // scheduled now (its CTAs take SMs as this grid's CTAs leave them).
   if (threadIdx.x == 0) grid_launch_dependents();
 #ifdef GEMM_WS_DEBUG
-  // Stamps per CTA: entry, start of work (after the previous grid), exit.
-  if (p.phases && threadIdx.x == 0) {
-    p.phases[blockIdx.x * 8] = t_entry;
-    p.phases[blockIdx.x * 8 + 1] = global_timer_ns();
-  }
+  // Stamps per CTA: entry, start of work (after the previous grid; taken by
+  // the A producer before its first copy), exit.
+  if (p.phases && threadIdx.x == 0) p.phases[blockIdx.x * 8] = t_entry;
 #endif
 
   if (warp == WARP_TMA || warp == WARP_TMA_B) {
