@@ -369,7 +369,8 @@ def other_workloads(g, dev, stream, steps: int = 30):
     """Informational figures for the other workloads (not the headline):
     TFLOP/s of the 4096^3 and ragged batched GEMMs, launch-to-launch latency
     of the 256^3 GEMM (latency-bound), and the HBM bandwidth of a skinny
-    8192 x 8192 x 64 GEMM (bound by writing D)."""
+    8192 x 8192 x 64 GEMM (bound by writing D), per call and replayed from a
+    CUDA graph."""
     out = {}
     # Both of these fit in L2 (96 MiB of operands at 4096^3), so they are
     # also timed with the L2 scrubbed before every call.
@@ -404,6 +405,11 @@ def other_workloads(g, dev, stream, steps: int = 30):
         if kind == "gbs":
             rec["gbs"] = round(w.algorithmic_bytes() / (ms * 1e-3) / 1e9, 1)
             rec["algorithmic_bytes"] = w.algorithmic_bytes()
+            # The same GEMM replayed from a CUDA graph: device time without
+            # the per-call host path between launches.
+            us = graph_replay_us(g, Ad, Bd, Cd, D, w, dev)
+            rec["us_per_gemm_graph_replay"] = round(us, 2)
+            rec["gbs_graph_replay"] = round(w.algorithmic_bytes() / (us * 1e-6) / 1e9, 1)
         out[w.name] = rec
         del A, B, C, Ad, Bd, Cd, D
     del scrub
