@@ -18,7 +18,7 @@ import oracle
 from async_pipelines_gb300 import gemm_ws, workloads
 from tests.debug_helpers import launch_shape
 from tests.gpu_helpers import bits_of, sample_rows
-from tests.numerics import assert_gemm_close
+from tests.numerics import assert_gemm_close, f64_to_bf16_bits
 
 pytestmark = pytest.mark.gpu
 
@@ -78,3 +78,28 @@ def test_phase_stamps_are_ordered(auto_debug):
     assert np.all(p[:, 0] > 0)
     assert np.all(p[:, 0] <= p[:, 1]) and np.all(p[:, 1] <= p[:, 2])
     assert p[:, 2].max() - p[:, 0].min() < 10_000_000   # well under 10 ms
+
+
+@pytest.mark.parametrize("M,N,K,L", [
+    (256, 256, 256, 1),    # two single-CTA tiles -> eight 64-column quarters
+    (300, 200, 520, 2),    # ragged: the last quarter of each tile straddles N or lies past it
+    (130, 72, 64, 1),      # N inside the first quarter; three quarters outside N
+    (1000, 776, 1024, 1),  # 32 tiles, 128 quarter units (a 4x wider launch than halves)
+])
+def test_quarter_units_bit_exact(auto_debug, M, N, K, L):
+    """Problems with at most a quarter as many tiles as clusters run every
+    tile as four 64-column units; integer inputs make the result exact, so
+    it must equal the oracle's bf16 bits, ragged edges included."""
+    cs, clusters, units, sk = launch_shape(auto_debug, M, N, K, L, streamout=False)
+    tiles = L * -(-M // (128 * cs)) * -(-N // 256)
+    assert sk == 0 and units == 4 * tiles and clusters == 4 * tiles
+    A, B, C = workloads.make_inputs(M, N, K, L, ("int", -3, 3), ("int", -4, 4), seed=M + N)
+    for beta, Cd in ((0.0, None), (1.5, C.cuda())):
+        D = torch.full((L, M, N), 9.0, dtype=torch.bfloat16, device="cuda")
+        auto_debug.run(A.cuda(), B.cuda(), Cd, D, 2.0, beta)
+        torch.cuda.synchronize()
+        ref = oracle.gemm(bits_of(A), bits_of(B), None if beta == 0 else bits_of(C),
+                          M, N, K, L, 2.0, beta)
+        np.testing.assert_array_equal(bits_of(D).reshape(L, M, N), f64_to_bf16_bits(ref))
+    # stream-out keeps 128-column units
+    assert launch_shape(auto_debug, M, N, K, L, streamout=True)[2] < 4 * tiles
