@@ -2,8 +2,10 @@
 // `can_implement` role of "sm90_gemm_tma_warpspecialized_cooperative.hpp"),
 // TMA descriptor encoding (cached per handle), the device workspace (counters,
 // status word, stream-K partials), the per-problem plan (tile configuration,
-// half-width tail units or stream-K pieces, persistent grid of at most the
-// co-resident clusters) and the launch, one CTA per SM.
+// half-width tail units, quarter-width units for tiny problems or stream-K
+// pieces, persistent grid of at most the co-resident clusters) and the
+// launches: the GEMM, one CTA per SM, and after split tiles the reduction of
+// their pieces.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>

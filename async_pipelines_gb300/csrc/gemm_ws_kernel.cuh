@@ -49,11 +49,11 @@
 // Every role walks the same static persistent unit sequence (next_unit:
 // cluster c takes tiles c, c + #clusters, ..., and, where the host planned
 // it, one equal piece of a tile's K range as its last unit), so the
-// scheduler needs no communication. The pieces of a tile combine their fp32
-// partials through a workspace in the epilogue (the fix-up step of the SM90
-// cooperative kernel). Every wait is bounded by a watchdog (global timer): on
-// expiry the kernel
-// records GEMM_WS_ERR_TIMEOUT in a status word, all roles leave their loops,
+// scheduler needs no communication. The pieces of a tile leave fp32 partials
+// in a workspace, which gemm_ws_reduce_kernel adds after the GEMM (the
+// separate-reduction form of the SM90 cooperative kernel's fix-up). Every
+// wait is bounded by a watchdog (global timer): on expiry the kernel records
+// GEMM_WS_ERR_TIMEOUT in a status word, all roles leave their loops,
 // in-flight copies are drained and TMEM is freed.
 #pragma once
 
@@ -220,7 +220,7 @@ struct Unit {
   int tile;    // tile index
   int kb0, kb1;        // ring stages [kb0, kb1) of the tile's K range
   int piece, pieces;   // piece `piece` of the `pieces` that share the K range (1: whole)
-  int sk_tile;         // index in the stream-K region (fix-up counters)
+  int sk_tile;         // index in the stream-K region
   int first_cluster;   // cluster that runs piece 0 (piece k runs on first_cluster + k)
   int id;              // unit number (trace index)
   int rev;             // the producer walks the k range from its end
@@ -1084,10 +1084,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_ws_kernel(const __grid_co
 
 // ------------------------------------------------------------ split reduction
 
-// The pieces of the split tiles, combined: one warp per 32 x 32 chunk of a
-// split tile's CTA part adds the chunk's fp32 partials of all S pieces in
-// piece order, then forms alpha * sum + beta * C, rounds it to bf16 and
-// stores D. It runs as its own kernel after the GEMM on the same stream (the
+// The pieces of the split tiles, combined: for every 32 x 32 chunk of a
+// split tile's CTA part, the chunk's fp32 partials of all S pieces are added
+// in piece order, then alpha * sum + beta * C is rounded to bf16 and stored
+// to D. It runs as its own kernel after the GEMM on the same stream (the
 // separate-reduction variant of the SM90 cooperative kernel's fix-up), so no
 // piece ever waits for another and the GEMM needs no co-resident clusters.
 struct ReduceParams {

@@ -2,14 +2,13 @@
 
 The library cuts the K range of the last tiles (all tiles, when there are at
 most half as many as clusters; else the tiles of a last, at most half-full
-wave) into equal pieces, each run by its own cluster as its last unit. The
-32 x 32 chunks of a tile are owned round-robin by its pieces; the others
-park fp32 partials of a chunk in the handle's workspace and count in, and
-the owner waits for them, adds them to its own accumulator in piece order
-(so the bits do not depend on which piece owns a chunk) and runs the
+wave) into equal pieces, each run by its own cluster as its last unit. Every
+piece writes its fp32 partial of the tile to the handle's workspace and waits
+for nothing; a reduction kernel that the call launches after the GEMM adds
+the pieces in piece order (the same bits on every run) and runs the
 alpha/beta epilogue. These tests check that the launch plan really splits,
-compare with the oracle, and check that back-to-back launches and graph
-replays (whose fix-up counters the kernel returns to zero) stay correct.
+compare with the oracle, and check that back-to-back launches, graph
+replays, work on another stream and the public kernel count stay correct.
 GEMM_WS_STREAM_K=2 splits shapes the cost model would run whole, down to
 one-stage pieces, so that many pieces, ragged K and a whole-tile part before
 the split tiles are covered at sizes the oracle checks quickly.
