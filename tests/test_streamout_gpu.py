@@ -100,8 +100,12 @@ def test_streamout_small(gw_each, M, N, K, L, beta):
 
 
 def test_streamout_matches_plain_run(gw_each):
-    """Stream-out leaves D identical to a plain run, bit for bit."""
+    """Stream-out leaves D identical to a plain run, bit for bit (when the
+    plain run's plan keeps whole K ranges, as by default at this shape: a
+    plan that splits K sums in another fp32 order)."""
     M, N, K, L = 512, 1024, 256, 1
+    if gw_each.kernels_per_run(M, N, K, L) != 1:
+        pytest.skip("the plain plan splits K here (GEMM_WS_STREAM_K forces it)")
     A, B, _ = workloads.make_inputs(M, N, K, L, ("uniform",), None, 33)
     Ad, Bd = A.cuda(), B.cuda()
     D0 = torch.empty(L, M, N, dtype=torch.bfloat16, device="cuda")
