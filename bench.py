@@ -315,41 +315,57 @@ def time_e2e_serial(g, w, Ah, Bh, Ch, Ad, Bd, Cd, D, stream, warmup, steps, worl
     return time_launches(step, steps, stream)
 
 
-def time_e2e_pipelined(g, w, Ah, Bh, Ch, dev, comp, warmup, steps, world):
+def time_e2e_pipelined(g, w, Ah, Bh, Ch, dev, comp, warmup, steps, world, one_copy_stream=False):
     """ms per step with copy-in of step i+1 and copy-out of step i-1 overlapping
-    the GEMM of step i (two device buffer sets, events between the streams)."""
+    the GEMM of step i (two device buffer sets, events between the streams).
+    one_copy_stream: both copy directions on one stream, so they overlap the
+    GEMMs but not each other (on some hosts the two directions at once are
+    slower than one after the other)."""
     bufs = [tuple(torch.empty(t.shape, dtype=t.dtype, device=dev) for t in (Ah, Bh, Ch))
             + (torch.empty(w.L, w.M, w.N, dtype=torch.bfloat16, device=dev),)
             for _ in range(2)]
     Dh = [torch.empty(w.L, w.M, w.N, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
-    cin, cout = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    cin = torch.cuda.Stream(device=dev)
+    cout = cin if one_copy_stream else torch.cuda.Stream(device=dev)
     ev = {k: [torch.cuda.Event() for _ in range(2)] for k in ("in", "gemm", "out")}
 
-    def step(i):
+    def copy_in(i):
         b = i % 2
-        Ad, Bd, Cd, Dd = bufs[b]
         with torch.cuda.stream(cin):
             if i >= 2:
                 cin.wait_event(ev["gemm"][b])      # step i-2 no longer reads buffer set b
-            Ad.copy_(Ah, non_blocking=True)
-            Bd.copy_(Bh, non_blocking=True)
-            Cd.copy_(Ch, non_blocking=True)
+            for dst, src in zip(bufs[b][:3], (Ah, Bh, Ch)):
+                dst.copy_(src, non_blocking=True)
             ev["in"][b].record(cin)
+
+    def compute(i):
+        b = i % 2
+        Ad, Bd, Cd, Dd = bufs[b]
         comp.wait_event(ev["in"][b])
         if i >= 2:
             comp.wait_event(ev["out"][b])          # step i-2's D has been read back
         g.run(Ad, Bd, Cd, Dd, w.alpha, w.beta, stream=comp)
         ev["gemm"][b].record(comp)
+
+    def copy_out(i):
+        b = i % 2
         with torch.cuda.stream(cout):
             cout.wait_event(ev["gemm"][b])
-            Dh[b].copy_(Dd, non_blocking=True)
+            Dh[b].copy_(bufs[b][3], non_blocking=True)
             ev["out"][b].record(cout)
 
     def run(n):
+        # issue order in(0), in(1), gemm(0), out(0), in(2), gemm(1), out(1), ...:
+        # on one copy stream the copy-in of step i+1 then sits ahead of the
+        # copy-out of step i, so both overlap the GEMM of step i.
         cin.wait_stream(comp)
         cout.wait_stream(comp)
-        for i in range(n):
-            step(i)
+        for i in range(n + 1):
+            if i < n:
+                copy_in(i)
+            if i >= 1:
+                compute(i - 1)
+                copy_out(i - 1)
         comp.wait_stream(cin)
         comp.wait_stream(cout)
 
@@ -506,8 +522,21 @@ def run_ours(args, rank, world, local):
                                                    args.warmup, e2e_steps, world), world)
     del Ad, Bd, Cd, D
     torch.cuda.empty_cache()
-    e2e_ms = max_over_ranks(time_e2e_pipelined(g, w, Ah, Bh, Ch, dev, stream, args.warmup,
-                                               e2e_steps, world), world)
+    e2e_pipe_ms = max_over_ranks(time_e2e_pipelined(g, w, Ah, Bh, Ch, dev, stream, args.warmup,
+                                                    e2e_steps, world), world)
+    torch.cuda.empty_cache()
+    e2e_pipe1_ms = max_over_ranks(time_e2e_pipelined(g, w, Ah, Bh, Ch, dev, stream, args.warmup,
+                                                     e2e_steps, world, one_copy_stream=True),
+                                  world)
+    # The reported end-to-end figure is the fastest of the three schedules
+    # (every one copies every step's inputs in and its result out inside the
+    # timed region); all three are listed.
+    e2e_schedules = {
+        "serial: copy-in, GEMM, copy-out on one stream": e2e_serial_ms,
+        "2-deep pipeline: copy-in / GEMM / copy-out streams": e2e_pipe_ms,
+        "2-deep pipeline: one copy stream for both directions / GEMM stream": e2e_pipe1_ms,
+    }
+    e2e_schedule, e2e_ms = min(e2e_schedules.items(), key=lambda kv: kv[1])
     del Ah, Bh, Ch
     torch.cuda.empty_cache()
 
@@ -587,7 +616,8 @@ def run_ours(args, rank, world, local):
         "e2e": {"value": round(world * w.flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": UNIT,
                 "ms_per_step": round(e2e_ms, 4),
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "schedule": "2-deep pipeline: copy-in / GEMM / copy-out streams",
+                "schedule": e2e_schedule,
+                "schedules_ms_per_step": {k: round(v, 4) for k, v in e2e_schedules.items()},
                 "serial_value": round(world * w.flops / (e2e_serial_ms * 1e-3) / 1e12, 2),
                 "serial_ms_per_step": round(e2e_serial_ms, 4)},
         # this library's kernels in the timed region (the GEMM, and the
