@@ -40,8 +40,10 @@ struct gemm_ws {
   int group_m;                    // raster group: m-tiles walked per n step
   int max_pair_clusters;          // co-resident 2-CTA clusters of the pair kernel
   int stream_k;                   // 0 off, 1 where the cost model gains (default), 2 always
+  int sk_inline;                  // two-piece tiles: fix-up inside the GEMM (default 1)
   int k_snake;                    // every other unit of a cluster walks K backwards
-  uint32_t* work;                 // [0] stream-out counter, [1] status, [2] done count
+  uint32_t* work;                 // [0] stream-out counter, [1] status, [2] done count, then
+                                  // the in-kernel fix-up words (work_words)
   float* partial;                 // stream-K partials: num_sms parts of 128 x 256 fp32
   int last_cuda_error;
   unsigned long long timeout_ns;
@@ -60,6 +62,12 @@ namespace {
 constexpr int64_t kMaxDim = (int64_t{1} << 31) - 1;
 constexpr int64_t kMaxElems = int64_t{1} << 40;
 constexpr int kWorkWords = 4;   // counter [0], status [1], consumers done [2]
+
+// Words of a handle's work area: kWorkWords, then the in-kernel fix-up's
+// arrival counts and written flags (one per epilogue warp of each CTA).
+size_t work_words(int num_sms) {
+  return kWorkWords + 2 * static_cast<size_t>(num_sms) * gws::NUM_EPI_WARPS;
+}
 
 int cuda_fail(gemm_ws* h, cudaError_t e) {
   if (h) h->last_cuda_error = static_cast<int>(e);
@@ -213,11 +221,17 @@ int64_t cluster_capacity(const gemm_ws* h, int cs) {
 // order) have their K ranges cut into S equal pieces, each run by its own
 // cluster as that cluster's last unit; pieces with the same index sit at the
 // same k on every tile, so concurrent tiles still share A and B panels
-// through L2. Every piece writes its fp32 partial of the tile to its own
-// workspace part and waits for nothing; a reduction kernel that follows the
-// GEMM on the stream adds the pieces in piece order and runs the epilogue
-// for those tiles (the separate-reduction variant of the SM90 cooperative
-// kernel's fix-up), so the GEMM needs no co-resident clusters.
+// through L2. The pieces are added in piece order, and the alpha/beta
+// epilogue of those tiles runs after the sum:
+//  - two pieces (sk_inline): inside the GEMM. Per epilogue warp, the piece
+//    that arrives second takes the other's fp32 partial (written to the
+//    workspace and flagged) and runs the epilogue; it waits only for a piece
+//    that has already arrived, so the GEMM needs no co-resident clusters.
+//  - more pieces: every piece writes its partial and waits for nothing; a
+//    reduction kernel that follows the GEMM on the stream adds them (the
+//    separate-reduction variant of the SM90 cooperative kernel's fix-up).
+//    One piece adding all the others' partials would move S - 1 partials
+//    through one SM.
 //  - Few tiles (at most half as many as clusters): every tile, S =
 //    min(clusters / tiles, K / kMinShareK, kMaxSplit) (split-K).
 //  - Otherwise the tiles of the last, partial wave if it is at most half
@@ -232,10 +246,13 @@ constexpr int64_t kMinShareK = 1024;
 constexpr int64_t kMaxSplit = 16;
 constexpr int64_t kMaxSplitForced = 32;
 // Fix-up cost of a split tile, in ring stages of MMA work (~0.5-0.6 us each
-// on GB300): the pieces' partial writes, the reduction kernel after the GEMM
-// and a short piece's pipeline fill. Calibrated by timing: 10 splits
-// 1536^2 x 8192's tail (-1.8 %) and leaves 4096^3's to half-width tiles; 5 or
-// less also split 4096^3's, which then measured 4 % slower.
+// on GB300): the pieces' partial writes, their reduction (in the GEMM for two
+// pieces, else by the reduction kernel after it) and a short piece's
+// pipeline fill. Calibrated by timing: 10 splits 8192^3's and 1536^2 x
+// 8192's tails and leaves 4096^3's and 8192^2 x 4096's (32-stage tiles) to
+// half-width tiles. Split with the in-kernel fix-up, interleaved against
+// half-width tails: 8192^3 -0.6 %, 4096^3 +2.4 %, 8192^2 x 4096 +1.2 %; with
+// the reduction kernel 4096^3 was +4 %.
 constexpr double kPieceCostStages = 10.0;
 constexpr size_t kPartBytes = size_t{gws::BM} * gws::BN * sizeof(float);
 // Workspace: one partial part per CTA of a launch (each runs at most one
@@ -255,6 +272,7 @@ struct Plan {
   int64_t sk_first;    // first tile of the stream-K region (num_tiles: none)
   int64_t sk_split;    // pieces per tile of the region
   int64_t sk_clusters; // clusters running pieces
+  bool sk_inline;      // two-piece tiles fixed up inside the GEMM (no reduction kernel)
   int64_t clusters;    // persistent clusters launched
 };
 
@@ -297,6 +315,7 @@ Plan make_plan(const gemm_ws* h, int64_t M, int64_t N, int64_t K, int64_t L, boo
   q.sk_first = T;
   q.sk_split = 1;
   q.sk_clusters = 0;
+  q.sk_inline = false;
   // Quarter units for problems of so few tiles that four units per tile fit
   // on the GPU at once (a latency-bound launch: each SM's loads, MMAs and
   // epilogue shrink with the unit), unless split pieces are taken below.
@@ -322,11 +341,13 @@ Plan make_plan(const gemm_ws* h, int64_t M, int64_t N, int64_t K, int64_t L, boo
   if (S > (forced ? kMaxSplitForced : kMaxSplit)) S = forced ? kMaxSplitForced : kMaxSplit;
   if (S < 2) return quarters(q);
   const int64_t F = T - R, Pe = R * S;
+  const bool inl = S == 2 && h->sk_inline;
   const double sk_cost = static_cast<double>(F / P) + static_cast<double>((ns + S - 1) / S) / ns +
                          kPieceCostStages / static_cast<double>(ns);
   if (!forced && !(sk_cost < dp_cost - 1e-9)) return quarters(q);
   q.sk_first = F;
   q.sk_split = S;
+  q.sk_inline = inl;
   q.sk_clusters = Pe;
   q.num_full = T;
   q.num_units = F + Pe;
@@ -396,6 +417,8 @@ int launch(gemm_ws* h, const uint16_t* A, const uint16_t* B, const uint16_t* C, 
   p.sk_first = static_cast<int>(q.sk_first);
   p.sk_split = static_cast<int>(q.sk_split);
   p.partial = h->partial;
+  p.sk_inline = q.sk_inline ? 1 : 0;
+  p.sk_sync = q.sk_inline ? h->work + kWorkWords : nullptr;
   p.group_m = h->group_m;
   p.k_snake = h->k_snake;
   p.staging_tiles_m = static_cast<int>((M + gws::STAGING - 1) / gws::STAGING);
@@ -451,7 +474,7 @@ int launch(gemm_ws* h, const uint16_t* A, const uint16_t* B, const uint16_t* C, 
     }
   }
   if (e != cudaSuccess) return cuda_fail(h, e);
-  if (q.sk_first < q.num_tiles) {
+  if (q.sk_first < q.num_tiles && !q.sk_inline) {
     // The split tiles' pieces left fp32 partials; the reduction kernel adds
     // them and writes those tiles' D, next on the same stream.
     gws::ReduceParams rp;
@@ -515,6 +538,13 @@ int stream_k_from_env() {
     const int v = std::atoi(s);
     if (v == 0 || v == 2) return v;
   }
+  return 1;
+}
+
+// GEMM_WS_SK_INLINE=0 fixes two-piece tiles up with the reduction kernel, as
+// tiles of more pieces always are; default 1: inside the GEMM.
+int sk_inline_from_env() {
+  if (const char* s = std::getenv("GEMM_WS_SK_INLINE")) return std::atoi(s) == 0 ? 0 : 1;
   return 1;
 }
 
@@ -594,11 +624,13 @@ int gemm_ws_create(gemm_ws_t** out, int device) {
   h->pdl = pdl_from_env();
   h->group_m = group_m_from_env();
   h->stream_k = stream_k_from_env();
+  h->sk_inline = sk_inline_from_env();
   h->k_snake = k_snake_from_env();
   e = configure_kernels(h->num_sms, &h->max_pair_clusters);
   if (e == cudaSuccess && h->max_pair_clusters < 1) h->cta_group = 1;
-  if (e == cudaSuccess) e = cudaMalloc(&h->work, kWorkWords * sizeof(uint32_t));
-  if (e == cudaSuccess) e = cudaMemset(h->work, 0, kWorkWords * sizeof(uint32_t));
+  const size_t wbytes = work_words(h->num_sms) * sizeof(uint32_t);
+  if (e == cudaSuccess) e = cudaMalloc(&h->work, wbytes);
+  if (e == cudaSuccess) e = cudaMemset(h->work, 0, wbytes);
   // Stream-K workspace: one 128 x 256 fp32 partial per SM.
   if (e == cudaSuccess)
     e = cudaMalloc(&h->partial, static_cast<size_t>(h->num_sms) * kPartBytes);
@@ -668,11 +700,11 @@ int gemm_ws_query_status(gemm_ws_t* h, void* stream) {
   e = cudaMemcpy(&st, h->work + 1, sizeof st, cudaMemcpyDeviceToHost);
   if (e != cudaSuccess) return cuda_fail(h, e);
   if (st != 0) {
-    // Clear the status word, and the stream-out counters in case an aborted
-    // launch left them part-way, so the next launch starts from zero. The
-    // clear goes on `s` and is waited for, so it is complete before this
-    // returns whatever stream the next run uses.
-    e = cudaMemsetAsync(h->work, 0, kWorkWords * sizeof(uint32_t), s);
+    // Clear the status word, and the stream-out counters and fix-up words
+    // in case an aborted launch left them part-way, so the next launch
+    // starts from zero. The clear goes on `s` and is waited for, so it is
+    // complete before this returns whatever stream the next run uses.
+    e = cudaMemsetAsync(h->work, 0, work_words(h->num_sms) * sizeof(uint32_t), s);
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
     if (e != cudaSuccess) return cuda_fail(h, e);
   }
@@ -709,7 +741,7 @@ int gemm_ws_debug_phases(gemm_ws_t* h, unsigned long long* phases) {
 
 int gemm_ws_debug_launch_shape(gemm_ws_t* h, int64_t M, int64_t N, int64_t K, int64_t L,
                                int streamout, int* ctas_per_cluster, int* clusters,
-                               int* num_units, int* sk_tiles) {
+                               int* num_units, int* sk_tiles, int* sk_pieces, int* sk_inline) {
   if (!h || !ctas_per_cluster || !clusters || !num_units || !sk_tiles || M <= 0 || N <= 0 ||
       K < 0 || L <= 0)
     return GEMM_WS_ERR_INVALID_ARG;
@@ -718,6 +750,8 @@ int gemm_ws_debug_launch_shape(gemm_ws_t* h, int64_t M, int64_t N, int64_t K, in
   *num_units = static_cast<int>(q.num_units);
   *clusters = static_cast<int>(q.clusters);
   *sk_tiles = static_cast<int>(q.num_tiles - q.sk_first);
+  if (sk_pieces) *sk_pieces = static_cast<int>(q.sk_split);
+  if (sk_inline) *sk_inline = q.sk_inline ? 1 : 0;
   return GEMM_WS_OK;
 }
 
@@ -735,6 +769,7 @@ int gemm_ws_debug_schedule(int cta_group, int num_sms, int max_clusters, int str
   if (h.cta_group == 1) h.num_sms = max_clusters;
   h.group_m = 8;
   h.stream_k = stream_k;
+  h.sk_inline = 1;
   float dummy = 0.0f;
   h.partial = &dummy;   // only tested for null by the plan
   const Plan q = make_plan(&h, M, N, K, L, streamout != 0);
@@ -807,7 +842,7 @@ int gemm_ws_kernels_per_run(gemm_ws_t* h, int64_t M, int64_t N, int64_t K, int64
     return -GEMM_WS_ERR_INVALID_ARG;
   if (M * N * L == 0) return 0;
   const Plan q = make_plan(h, M, N, K, L, streamout != 0);
-  return q.sk_first < q.num_tiles ? 2 : 1;
+  return q.sk_first < q.num_tiles && !q.sk_inline ? 2 : 1;
 }
 
 }  // extern "C"

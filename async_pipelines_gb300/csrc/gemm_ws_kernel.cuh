@@ -78,6 +78,13 @@ constexpr int STAGING = 128;             // stream-out tile edge
 constexpr int SUB_PER_STAGING = STAGING / EPI_N;
 constexpr int SUB_PER_PART = BN / EPI_N;   // subtiles (32 x 32 chunks per lane quarter) of a part
 constexpr int CHUNK_FLOATS = 32 * EPI_N;      // one 32 x 32 fp32 partial chunk
+constexpr uint32_t CHUNK_BYTES = CHUNK_FLOATS * 4;
+// A piece's partial, per epilogue warp (lane quarter q, subtiles j = hf + 2k):
+// the warp's four chunks k = 0..3 lie together, so that one bulk copy moves
+// them; chunk (q, j) of a CTA's part starts at this many floats.
+__host__ __device__ __forceinline__ int part_chunk_offset(int q, int j) {
+  return ((q * 2 + (j & 1)) * 4 + (j >> 1)) * CHUNK_FLOATS;
+}
 constexpr int PART_FLOATS = 4 * SUB_PER_PART * CHUNK_FLOATS;   // a CTA's 128 x 256 partial
 constexpr int WARP_TMA = 0;
 constexpr int WARP_MMA = 1;
@@ -103,7 +110,8 @@ constexpr int BAR_C_FULL = BAR_ACC_EMPTY + ACC_BUFS;          // [epilogue warp]
 constexpr int BAR_D_FULL = BAR_C_FULL + NUM_EPI_WARPS;
 constexpr int BAR_D_EMPTY = BAR_D_FULL + EPI_SLOTS_NOC;
 constexpr int BAR_MMA_DRAIN = BAR_D_EMPTY + EPI_SLOTS_NOC;
-constexpr int NUM_BARS = BAR_MMA_DRAIN + 1;
+constexpr int BAR_FIX = BAR_MMA_DRAIN + 1;                      // [epilogue warp][chunk]
+constexpr int NUM_BARS = BAR_FIX + NUM_EPI_WARPS * 4;
 
 template <int CG>
 struct Cfg {
@@ -165,6 +173,12 @@ struct Params {
   int sk_first;
   int sk_split;
   float* partial;                // piece partials: [cluster][CTA][chunk] x 1024 fp32
+  // In-kernel fix-up of two-piece tiles (sk_inline, sk_split == 2): per
+  // epilogue warp of each CTA, an arrival count per split tile and a
+  // partial-written flag per piece (see sk_arrival_word / sk_written_word);
+  // all zero at launch, and the kernel leaves them zero again.
+  int sk_inline;
+  uint32_t* sk_sync;
   int group_m;                   // raster: tiles walk group_m m-tiles per n step
   int k_snake;                   // 1: every other unit of a cluster walks K backwards
   int staging_tiles_m;           // ceil(M / 128)
@@ -260,6 +274,20 @@ __host__ __device__ __forceinline__ Unit unit_coords(const Params& p, int u) {
 // Workspace slot of piece k of a stream-K tile: the cluster that runs it.
 __host__ __device__ __forceinline__ int sk_slot(const Params&, const Unit& w, int k) {
   return w.first_cluster + k;
+}
+
+// In-kernel fix-up words of epilogue warp e of CTA `rank` (cs CTAs per
+// cluster): the arrival count of split tile r (its sk_tile), then the flag
+// that the piece in workspace slot s has written its partial. Each area has
+// gridDim.x * NUM_EPI_WARPS words (r and s are below the cluster count).
+__device__ __forceinline__ uint32_t* sk_arrival_word(const Params& p, int cs, int r,
+                                                     uint32_t rank, int e) {
+  return p.sk_sync + (static_cast<size_t>(r) * cs + rank) * NUM_EPI_WARPS + e;
+}
+__device__ __forceinline__ uint32_t* sk_written_word(const Params& p, int cs, int s,
+                                                     uint32_t rank, int e) {
+  return p.sk_sync + static_cast<size_t>(gridDim.x) * NUM_EPI_WARPS +
+         (static_cast<size_t>(s) * cs + rank) * NUM_EPI_WARPS + e;
 }
 
 // The i-th unit of cluster c (of `clusters`), in the order every role of the
@@ -432,6 +460,35 @@ __device__ __forceinline__ bool warp_wait_spin(uint32_t bar, uint32_t parity,
   if ((threadIdx.x & 31) == 0) ok = wait_spin<true>(bar, parity, wd) ? 1u : 0u;
   ok = __shfl_sync(0xffffffffu, ok, 0);
   if (ok) (void)mbar_try_wait_cluster(bar, parity);
+  __syncwarp();
+  return ok != 0;
+}
+
+// Warp-uniform bounded wait for a flag in global memory that another CTA
+// sets with release semantics (the in-kernel fix-up's partial-written flag):
+// lane 0 polls with acquire loads; on success every lane loads the flag once
+// more with acquire, so each thread itself is ordered after the writer's
+// partial stores.
+__device__ __noinline__ bool flag_wait_slow(const uint32_t* f, const Watchdog& wd) {
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (ld_acquire_gpu(f) != 0u) return true;
+    if ((it & 63) == 0) {
+      if (*wd.abort) return false;
+      if (global_timer_ns() - t0 > wd.limit_ns) {
+        *wd.abort = 1;
+        atomicExch(wd.status, STATUS_TIMEOUT);
+        return false;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ bool warp_wait_flag(const uint32_t* f, const Watchdog& wd) {
+  uint32_t ok = 0;
+  if ((threadIdx.x & 31) == 0) ok = (ld_acquire_gpu(f) != 0u || flag_wait_slow(f, wd)) ? 1u : 0u;
+  ok = __shfl_sync(0xffffffffu, ok, 0);
+  if (ok) (void)ld_acquire_gpu(f);
   __syncwarp();
   return ok != 0;
 }
@@ -828,8 +885,58 @@ __device__ __forceinline__ void epilogue_role(const Params& p, uint32_t sbase, u
 #endif
     const uint32_t tacc = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + b * BN;
 
+    // In-kernel fix-up of a two-piece tile: for this warp's chunks, the piece
+    // whose warp arrives second adds the other piece's partial and runs the
+    // epilogue; the first one writes its partial and flags it. The second
+    // only ever waits for a piece that has already arrived (which writes
+    // without waiting for anything), so no two clusters need to be resident
+    // at once.
+    bool reduce = false;
+    if (split && p.sk_inline && hf < nsub) {
+      uint32_t before = 0;
+      if (lane == 0) before = atomicAdd(sk_arrival_word(p, C::CS, w.sk_tile, rank, e), 1u);
+      before = __shfl_sync(0xffffffffu, before, 0);
+      reduce = before == static_cast<uint32_t>(w.pieces - 1);
+#ifdef GEMM_WS_DEBUG
+      if (p.phases && e == 0 && lane == 0 && reduce) p.phases[blockIdx.x * 8 + 4] = global_timer_ns();
+#endif
+    }
+    // The other piece's fp32 partial of this warp's chunks (reducer only),
+    // bulk-copied into this warp's share of the ring's shared memory, which
+    // the piece (its cluster's last unit) no longer loads into.
+    const int nchunk = hf < nsub ? min(4, (nsub - hf + 1) / 2) : 0;
+    const uint8_t* other = nullptr;
+    uint8_t* fixbuf = smem + C::OFF_A + e * (4 * CHUNK_BYTES);
+    if (reduce) {
+      const int op = 1 - w.piece;
+      if (p.has_c) issue_c(hf);
+      uint32_t* written = sk_written_word(p, C::CS, sk_slot(p, w, op), rank, e);
+      if (!warp_wait_flag(written, wd)) break;
+#ifdef GEMM_WS_DEBUG
+      if (p.phases && e == 0 && lane == 0) p.phases[blockIdx.x * 8 + 5] = global_timer_ns();
+#endif
+      if (lane == 0) {
+        // Both pieces have arrived and the other is done with its flag: the
+        // words go back to zero for the next launch.
+        *sk_arrival_word(p, C::CS, w.sk_tile, rank, e) = 0u;
+        *written = 0u;
+        fence_proxy_async_global();   // the flag's acquire, then the bulk (async-proxy) read
+        const float* src = p.partial +
+                           (static_cast<size_t>(sk_slot(p, w, op)) * C::CS + rank) * PART_FLOATS +
+                           part_chunk_offset(q, hf);
+        // One copy (and barrier) per chunk, so the first subtile's sum can
+        // start while the later chunks are still on their way.
+        for (int k = 0; k < nchunk; ++k) {
+          mbar_arrive_expect_tx(bar(BAR_FIX + 4 * e + k), CHUNK_BYTES);
+          bulk_load_1d(smem_addr(fixbuf + k * CHUNK_BYTES), src + k * CHUNK_FLOATS, CHUNK_BYTES,
+                       bar(BAR_FIX + 4 * e + k));
+        }
+      }
+      other = fixbuf;
+    }
+
     bool ok = true;
-    if (!split) {
+    if (!split || reduce) {
       if (nsub == 0) release_acc();   // this CTA's rows lie outside M x N
       for (int j = hf; j < nsub; j += 2) {
         uint32_t acc[32];
@@ -842,8 +949,33 @@ __device__ __forceinline__ void epilogue_role(const Params& p, uint32_t sbase, u
         }
         if (j + 2 >= nsub) release_acc();
         float v[32];
+        if (other) {
+          // The two partials in piece order, from zero: the same sum, bit
+          // for bit, as the separate reduction kernel's.
+          const bool first = w.piece == 0;
+          if (!warp_wait_spin(bar(BAR_FIX + 4 * e + (j >> 1)), 0, wd)) {
+            // The copies land before the CTA exits.
+            if (lane == 0)
+              for (int k = j >> 1; k < nchunk; ++k) wait_drain(bar(BAR_FIX + 4 * e + k), 0);
+            ok = false;
+            break;
+          }
+          const float4* oc = reinterpret_cast<const float4*>(other + (j >> 1) * CHUNK_BYTES) + lane;
 #pragma unroll
-        for (int x = 0; x < 32; ++x) v[x] = p.alpha * __uint_as_float(acc[x]);
+          for (int c = 0; c < 8; ++c) {
+            const float4 o = oc[c * 32];
+            const float o4[4] = {o.x, o.y, o.z, o.w};
+#pragma unroll
+            for (int x = 0; x < 4; ++x) {
+              const float mine = __uint_as_float(acc[4 * c + x]);
+              const float s0 = first ? mine : o4[x], s1 = first ? o4[x] : mine;
+              v[4 * c + x] = p.alpha * ((0.0f + s0) + s1);
+            }
+          }
+        } else {
+#pragma unroll
+          for (int x = 0; x < 32; ++x) v[x] = p.alpha * __uint_as_float(acc[x]);
+        }
         if (!finish_subtile(j, v, j + 2 < nsub ? j + 2 : -1)) {
           ok = false;
           break;
@@ -852,32 +984,51 @@ __device__ __forceinline__ void epilogue_role(const Params& p, uint32_t sbase, u
     } else {
       // A piece of the tile's K range (every piece of a tile runs on its own
       // cluster, as that cluster's last unit): this warp's fp32 partial of
-      // each of its 32 x 32 chunks (TMEM lane quarter q, subtiles j = hf +
-      // 2k) goes to the piece's workspace part, in TMEM register order
-      // (float4 c of lane r at [c][r], so a warp's store is 512 contiguous
-      // bytes). Nothing here waits for another piece: the reduction kernel
-      // that follows on the stream adds the pieces and runs the epilogue (the
+      // its 32 x 32 chunks (TMEM lane quarter q, subtiles j = hf + 2k) goes
+      // to the piece's workspace part, each chunk in TMEM register order
+      // (float4 c of lane r at [c][r]), the warp's chunks together
+      // (part_chunk_offset). It passes through this warp's share of the
+      // ring's shared memory (no more loads land there: the piece is its
+      // cluster's last unit) and leaves in one bulk copy. Nothing here waits
+      // for another piece. The partial is added either by the other piece's
+      // warp (in-kernel fix-up, which this warp signals through its written
+      // flag) or by the reduction kernel that follows on the stream (the
       // separate-reduction variant of the SM90 cooperative kernel's fix-up).
-      float* part = p.partial + (static_cast<size_t>(sk_slot(p, w, w.piece)) * C::CS + rank) *
-                                    PART_FLOATS;
-#pragma unroll 1
-      for (int k = 0; k < SUB_PER_PART / 2; ++k) {
-        const int j = hf + 2 * k;
-        if (j >= nsub) break;   // outside N (or this CTA's rows outside M)
+      for (int k = 0; k < nchunk; ++k) {
         uint32_t acc[32];
-        tmem_ld_32x32b_x32(tacc + j * EPI_N, acc);
+        tmem_ld_32x32b_x32(tacc + (hf + 2 * k) * EPI_N, acc);
         tmem_wait_ld();
-        float4* dst = reinterpret_cast<float4*>(part + (q * SUB_PER_PART + j) * CHUNK_FLOATS);
+        float4* dst = reinterpret_cast<float4*>(fixbuf + k * CHUNK_BYTES) + lane;
 #pragma unroll
         for (int c = 0; c < 8; ++c)
-          __stcg(dst + c * 32 + lane,
-                 make_float4(__uint_as_float(acc[4 * c]), __uint_as_float(acc[4 * c + 1]),
-                             __uint_as_float(acc[4 * c + 2]), __uint_as_float(acc[4 * c + 3])));
+          dst[c * 32] = make_float4(__uint_as_float(acc[4 * c]), __uint_as_float(acc[4 * c + 1]),
+                                    __uint_as_float(acc[4 * c + 2]), __uint_as_float(acc[4 * c + 3]));
       }
       release_acc();
 #ifdef GEMM_WS_DEBUG
       if (p.phases && e == 0 && lane == 0) p.phases[blockIdx.x * 8 + 3] = global_timer_ns();
 #endif
+      if (nchunk > 0) {
+        fence_proxy_async_smem();   // generic shared-memory writes -> the bulk copy
+        __syncwarp();
+        if (lane == 0) {
+          float* part = p.partial +
+                        (static_cast<size_t>(sk_slot(p, w, w.piece)) * C::CS + rank) * PART_FLOATS +
+                        part_chunk_offset(q, hf);
+          bulk_store_1d(part, smem_addr(fixbuf), nchunk * CHUNK_BYTES);
+          bulk_commit();
+          if (p.sk_inline) {
+            // The partial is in global memory, then the flag (release, gpu
+            // scope); the reduction kernel instead runs after this grid.
+            bulk_wait<0>();
+            fence_proxy_async_global();
+            st_release_gpu(sk_written_word(p, C::CS, sk_slot(p, w, w.piece), rank, e), 1u);
+#ifdef GEMM_WS_DEBUG
+            if (p.phases && e == 0) p.phases[blockIdx.x * 8 + 6] = global_timer_ns();
+#endif
+          }
+        }
+      }
     }
     if (!ok) break;
 #ifdef GEMM_WS_DEBUG
@@ -1008,6 +1159,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_ws_kernel(const __grid_co
       mbar_init(bar(BAR_D_EMPTY + s), 1);
     }
     mbar_init(bar(BAR_MMA_DRAIN), 1);
+    for (int i = 0; i < NUM_EPI_WARPS * 4; ++i) mbar_init(bar(BAR_FIX + i), 1);
     *abort_flag = 0;
     fence_mbar_init();
     if (p.num_kb > 0) {
@@ -1133,7 +1285,7 @@ __global__ void __launch_bounds__(REDUCE_THREADS)
   const float4* src = reinterpret_cast<const float4*>(
                           p.partial + (static_cast<size_t>(r) * p.sk_split * p.cs + rank) *
                                           PART_FLOATS +
-                          (q * SUB_PER_PART + j) * CHUNK_FLOATS) +
+                          part_chunk_offset(q, j)) +
                       t;
   const size_t piece_stride = static_cast<size_t>(p.cs) * PART_FLOATS / 4;   // float4s
   float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);

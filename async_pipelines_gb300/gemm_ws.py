@@ -100,7 +100,7 @@ def load_debug_library():
         ip = ctypes.POINTER(ctypes.c_int)
         lib.gemm_ws_debug_launch_shape.argtypes = [ctypes.c_void_p, ctypes.c_int64,
                                                    ctypes.c_int64, ctypes.c_int64,
-                                                   ctypes.c_int64, ctypes.c_int, ip, ip, ip, ip]
+                                                   ctypes.c_int64, ctypes.c_int, ip, ip, ip, ip, ip, ip]
         lib.gemm_ws_debug_launch_shape.restype = ctypes.c_int
         i64 = ctypes.c_int64
         lib.gemm_ws_debug_schedule.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int,

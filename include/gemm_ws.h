@@ -26,8 +26,9 @@
  * Ownership: every data pointer is a borrowed DEVICE pointer on the handle's
  * device; the caller owns it and keeps it alive until the stream work ends.
  * The handle owns only its device workspace: the stream-out sequence
- * counter, a status word, a completion count, and the split-K area (one
- * 128 x 256 fp32 partial per SM, 128 KiB per SM).
+ * counter, a status word, a completion count, the split-K area (one
+ * 128 x 256 fp32 partial per SM, 128 KiB per SM) and the split tiles'
+ * arrival counts and written flags (64 bytes per SM).
  * The kernel returns every counter to zero before it ends, so runs need no
  * clearing between them; runs on one handle that overlap on the GPU (e.g. on
  * two streams) race on that workspace: serialise them or use one handle per
@@ -97,10 +98,17 @@ int gemm_ws_destroy(gemm_ws_t* h);
  * tiles is at most half full, those tiles' K ranges may be cut into 2..16
  * equal pieces of >= 1024 that run on separate clusters (chosen by a host
  * cost model); acc is then the sum, in piece order, of the pieces' fp32
- * partials (deterministic: the same bits on every run). The pieces write
- * their partials and wait for nothing; a second, small kernel that the call
- * launches after the GEMM on the same stream adds them and writes those
- * tiles' D, so the call works on a GPU shared with other kernels too.
+ * partials (deterministic: the same bits on every run). With two pieces the
+ * GEMM kernel adds them itself: per epilogue warp, the piece that arrives
+ * second waits for the other's partial (written to the workspace and
+ * flagged), adds it and writes D; it waits only for a piece that has already
+ * arrived. With more pieces, every piece writes its partial and waits for
+ * nothing; a second, small kernel that the call launches after the GEMM on
+ * the same stream adds them and writes those tiles' D. Both give the same
+ * bits, and neither needs the pieces to run at the same time, so the call
+ * works on a GPU shared with other kernels too. GEMM_WS_SK_INLINE=0 in the
+ * environment at gemm_ws_create sends two-piece tiles to the reduction
+ * kernel as well.
  * GEMM_WS_STREAM_K in the environment at gemm_ws_create sets this per
  * handle: 0 off, 1 (default) by the cost model, 2 wherever the shape allows
  * (pieces down to one ring stage). gemm_ws_run_streamout never splits.
@@ -168,8 +176,8 @@ const char* gemm_ws_status_string(int status);
 int64_t gemm_ws_streamout_tiles(int64_t M, int64_t N, int64_t L);
 
 /* Kernels that a run of this problem on this handle launches on its stream:
- * 1, or 2 when some tiles are split into K pieces (the GEMM, then the
- * reduction of the pieces); 0 for an empty problem (M*N*L == 0); negative
+ * 1, or 2 when some tiles are split into more than two K pieces (the GEMM,
+ * then the reduction of the pieces); 0 for an empty problem (M*N*L == 0); negative
  * (a gemm_ws_status, negated) for invalid sizes or a NULL handle. streamout:
  * nonzero for gemm_ws_run_streamout, which never splits. Host arithmetic
  * only, the same plan the run makes; useful for counting launches or sizing

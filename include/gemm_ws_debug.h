@@ -52,14 +52,16 @@ int gemm_ws_debug_phases(gemm_ws_t* h, unsigned long long* phases);
 /* The launch the handle would make for an M x N x K x L problem (streamout:
  * nonzero for gemm_ws_run_streamout, 0 for gemm_ws_run): CTAs per cluster
  * (1 or 2), number of clusters (persistent CTA groups),
- * an upper bound of the work-unit ids (size the trace buffer with it) and
- * the number of tiles in the stream-K region (0: every tile runs whole or
- * as two halves). Host arithmetic only.
+ * an upper bound of the work-unit ids (size the trace buffer with it), the
+ * number of tiles in the stream-K region (0: every tile runs whole or in
+ * parts), and, where the last two pointers are not NULL, the pieces per
+ * split tile (1: none) and whether the GEMM kernel itself adds them (1) or
+ * the reduction kernel does (0). Host arithmetic only.
  * Returns GEMM_WS_OK or GEMM_WS_ERR_INVALID_ARG (null output pointer, M, N or
  * L below 1, K below 0). */
 int gemm_ws_debug_launch_shape(gemm_ws_t* h, int64_t M, int64_t N, int64_t K, int64_t L,
                                int streamout, int* ctas_per_cluster, int* clusters,
-                               int* num_units, int* sk_tiles);
+                               int* num_units, int* sk_tiles, int* sk_pieces, int* sk_inline);
 
 /* The whole persistent schedule of a launch, on the host, without a handle
  * or a GPU: the plan the library makes for a device with `num_sms` SMs on

@@ -34,9 +34,21 @@ def launch_shape(g: gemm_ws.GemmWS, M: int, N: int, K: int, L: int, streamout: b
     """(CTAs per cluster, clusters, unit-id bound, stream-K tiles) of the handle's launch."""
     cg, cl, nu, ks = ctypes.c_int(), ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
     rc = g.lib.gemm_ws_debug_launch_shape(g.handle, M, N, K, L, int(streamout), ctypes.byref(cg),
-                                          ctypes.byref(cl), ctypes.byref(nu), ctypes.byref(ks))
+                                          ctypes.byref(cl), ctypes.byref(nu), ctypes.byref(ks),
+                                          None, None)
     assert rc == gemm_ws.OK
     return cg.value, cl.value, nu.value, ks.value
+
+
+def split_plan(g: gemm_ws.GemmWS, M: int, N: int, K: int, L: int):
+    """(pieces per split tile, 1 if the GEMM kernel adds them itself / 0 if
+    the reduction kernel does) of the handle's gemm_ws_run launch."""
+    cg, cl, nu, ks, sp, si = (ctypes.c_int() for _ in range(6))
+    rc = g.lib.gemm_ws_debug_launch_shape(g.handle, M, N, K, L, 0, ctypes.byref(cg),
+                                          ctypes.byref(cl), ctypes.byref(nu), ctypes.byref(ks),
+                                          ctypes.byref(sp), ctypes.byref(si))
+    assert rc == gemm_ws.OK
+    return sp.value, si.value
 
 
 def configure(g: gemm_ws.GemmWS, fault: int, trace_ptr=None):

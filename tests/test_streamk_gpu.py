@@ -2,13 +2,16 @@
 
 The library cuts the K range of the last tiles (all tiles, when there are at
 most half as many as clusters; else the tiles of a last, at most half-full
-wave) into equal pieces, each run by its own cluster as its last unit. Every
-piece writes its fp32 partial of the tile to the handle's workspace and waits
-for nothing; a reduction kernel that the call launches after the GEMM adds
-the pieces in piece order (the same bits on every run) and runs the
-alpha/beta epilogue. These tests check that the launch plan really splits,
-compare with the oracle, and check that back-to-back launches, graph
-replays, work on another stream and the public kernel count stay correct.
+wave) into equal pieces, each run by its own cluster as its last unit. With
+two pieces, the piece whose epilogue warp arrives second adds the other's
+fp32 partial (written to the handle's workspace and flagged) and runs the
+alpha/beta epilogue itself; with more, every piece writes its partial and a
+reduction kernel that the call launches after the GEMM adds them. Either way
+the pieces are added in piece order (the same bits on every run, and the
+same bits from both fix-ups), and no piece waits for one that has not
+started. These tests check that the launch plan really splits, compare with
+the oracle, and check that back-to-back launches, graph replays, work on
+another stream and the public kernel count stay correct.
 GEMM_WS_STREAM_K=2 splits shapes the cost model would run whole, down to
 one-stage pieces, so that many pieces, ragged K and a whole-tile part before
 the split tiles are covered at sizes the oracle checks quickly.
@@ -23,7 +26,7 @@ import torch
 
 import oracle
 from async_pipelines_gb300 import gemm_ws, workloads
-from tests.debug_helpers import debug_handle, launch_shape
+from tests.debug_helpers import debug_handle, launch_shape, split_plan
 from tests.gpu_helpers import bits_of, sample_rows, to_dev
 from tests.numerics import assert_gemm_close, f64_to_bf16_bits
 
@@ -33,11 +36,12 @@ CONFIGS = [2, 1]
 IDS = ["cta_pair", "cta_single"]
 
 
-def _handle(cg, stream_k, lib=None):
-    keys = ("GEMM_WS_CTA_GROUP", "GEMM_WS_STREAM_K")
+def _handle(cg, stream_k, lib=None, inline=1):
+    keys = ("GEMM_WS_CTA_GROUP", "GEMM_WS_STREAM_K", "GEMM_WS_SK_INLINE")
     old = {k: os.environ.get(k) for k in keys}
     os.environ["GEMM_WS_CTA_GROUP"] = str(cg)
     os.environ["GEMM_WS_STREAM_K"] = str(stream_k)
+    os.environ["GEMM_WS_SK_INLINE"] = str(inline)
     try:
         return gemm_ws.GemmWS(0, lib=lib)
     finally:
@@ -231,14 +235,18 @@ def test_plan_keeps_whole_tiles_where_it_should(cfg):
     assert sk_tiles(plan_auto, 1024, 1024, 1024, 1) == 0
 
 
-def test_split_gemm_beside_kernels_on_another_stream(cfg):
-    """Split pieces never wait for one another, so a split GEMM is correct
-    (and ends with status OK) while other work on another stream holds SMs:
-    cuBLAS GEMMs keep a second stream busy for the whole call (bounded: a
-    fixed number of library calls)."""
+@pytest.mark.parametrize("M,N,K,L,inline", [(512, 512, 16384, 1, 0), (1536, 1536, 8192, 1, 1)],
+                         ids=["reduction_kernel", "in_kernel"])
+def test_split_gemm_beside_kernels_on_another_stream(cfg, M, N, K, L, inline):
+    """No piece waits for one that has not started (a piece that adds
+    another's partial waits only for a piece that already arrived), so a
+    split GEMM is correct (and ends with status OK) while other work on
+    another stream holds SMs: cuBLAS GEMMs keep a second stream busy for the
+    whole call (bounded: a fixed number of library calls). Both fix-ups: the
+    reduction kernel (16 pieces per tile) and the in-kernel one (2)."""
     auto, _, plan, _ = cfg
-    M, N, K, L = 512, 512, 16384, 1
     assert sk_tiles(plan, M, N, K, L) > 0
+    assert split_plan(plan, M, N, K, L)[1] == inline
     A, B, C = workloads.make_inputs(M, N, K, L, ("uniform",), ("normal", 1.0), seed=55)
     Ad, Bd, Cd = A.cuda(), B.cuda(), C.cuda()
     X = torch.randn(4096, 4096, device="cuda", dtype=torch.bfloat16)
@@ -265,13 +273,69 @@ def test_split_gemm_beside_kernels_on_another_stream(cfg):
 
 def test_kernels_per_run_matches_the_plan(cfg):
     """The public launch count: 2 exactly where the plan splits tiles into
-    pieces (the GEMM and the reduction), 1 otherwise, 0 for empty problems."""
+    more than two pieces (the GEMM and the reduction), 1 otherwise (two
+    pieces are added inside the GEMM), 0 for empty problems."""
     auto, forced, plan_auto, plan_forced = cfg
     shapes = [(256, 256, 8192, 1), (1024, 1024, 1024, 1), (8192, 8192, 8192, 1),
-              (4096, 4096, 4096, 1), (200, 296, 16384, 3), (4096, 2560, 512, 1)]
+              (4096, 4096, 4096, 1), (200, 296, 16384, 3), (4096, 2560, 512, 1),
+              (1536, 1536, 8192, 1)]
+    seen = set()
     for g, plan in ((auto, plan_auto), (forced, plan_forced)):
         for M, N, K, L in shapes:
-            want = 2 if sk_tiles(plan, M, N, K, L) > 0 else 1
+            pieces, inline = split_plan(plan, M, N, K, L)
+            split = sk_tiles(plan, M, N, K, L) > 0
+            assert inline == (split and pieces == 2), (M, N, K, L)
+            want = 2 if split and not inline else 1
+            if split:
+                seen.add(inline)
             assert g.kernels_per_run(M, N, K, L) == want, (M, N, K, L)
             assert g.kernels_per_run(M, N, K, L, streamout=True) == 1
         assert g.kernels_per_run(0, 64, 64, 1) == 0
+    assert seen == {0, 1}   # both fix-ups occur among these shapes
+
+
+def _in_kernel_cases(cg):
+    # Forced plans whose split tiles have exactly two pieces: M x N tiles
+    # between a third and a half of the cluster count (76 CTA pairs / 152
+    # single CTAs); ragged edges and C included.
+    if cg == 2:
+        return [(1536, 1536, 4096, 1, 1.0, 0.0), (1400, 1480, 3000, 1, 1.5, -0.5)]
+    return [(1024, 2048, 4096, 1, 1.0, 0.0), (1000, 1960, 3000, 1, 1.5, -0.5)]
+
+
+def test_in_kernel_fixup_equals_reduction_kernel(cfg):
+    """Two-piece tiles: the in-kernel fix-up and the reduction kernel add the
+    same two partials in the same order, so D is bit-identical, and both
+    match the oracle; the fix-up words return to zero (a second launch is
+    again bit-identical)."""
+    auto, forced, plan_auto, plan_forced = cfg
+    cg = launch_shape(plan_forced, 1536, 1536, 4096, 1, streamout=False)[0]
+    sep = _handle(cg, 2, inline=0)
+    sep_plan = _handle(cg, 2, gemm_ws.load_debug_library(), inline=0)
+    try:
+        for (M, N, K, L, alpha, beta) in _in_kernel_cases(cg):
+            assert sk_tiles(plan_forced, M, N, K, L) > 0
+            assert split_plan(plan_forced, M, N, K, L) == (2, 1), (M, N, K, L)
+            assert split_plan(sep_plan, M, N, K, L) == (2, 0), (M, N, K, L)
+            assert forced.kernels_per_run(M, N, K, L) == 1
+            assert sep.kernels_per_run(M, N, K, L) == 2
+            cd = ("normal", 1.0) if beta != 0 else None
+            A, B, C = workloads.make_inputs(M, N, K, L, ("uniform",), cd, seed=M + K)
+            Ad, Bd, Cd = to_dev(A), to_dev(B), to_dev(C)
+            outs = []
+            for g in (forced, sep, forced):
+                D = torch.full((L, M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+                g.run(Ad, Bd, Cd, D, alpha, beta)
+                outs.append(D)
+            torch.cuda.synchronize()
+            for D in outs[1:]:
+                assert torch.equal(D.view(torch.int16), outs[0].view(torch.int16)), (M, N, K, L)
+            rows = sample_rows(M, L, 24, seed=K)
+            ref = oracle.gemm_rows(bits_of(A), bits_of(B), None if C is None else bits_of(C),
+                                   M, N, K, L, alpha, beta, rows=rows)
+            assert_gemm_close(bits_of(outs[0]).reshape(L * M, N)[rows], ref, K,
+                              f"in-kernel fix-up {M}x{N}x{K}")
+        assert sep.query_status() == gemm_ws.OK
+    finally:
+        sep.close()
+        sep_plan.close()
