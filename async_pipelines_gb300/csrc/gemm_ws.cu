@@ -727,7 +727,7 @@ const char* gemm_ws_status_string(int status) {
 
 #ifdef GEMM_WS_DEBUG
 int gemm_ws_debug_configure(gemm_ws_t* h, int fault, unsigned long long* trace) {
-  if (!h || fault < 0 || fault > 1) return GEMM_WS_ERR_INVALID_ARG;
+  if (!h || fault < 0 || fault > 2) return GEMM_WS_ERR_INVALID_ARG;
   h->debug_fault = fault;
   h->trace = trace;
   return GEMM_WS_OK;

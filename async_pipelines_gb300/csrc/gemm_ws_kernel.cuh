@@ -195,7 +195,8 @@ struct Params {
   uint32_t* status;              // watchdog status word
   unsigned long long timeout_ns; // bound of every single wait
 #ifdef GEMM_WS_DEBUG
-  int debug_fault;               // 1: the stream-out consumer takes no tile
+  int debug_fault;               // 1: the stream-out consumer takes no tile; 2: split pieces
+                                 // never flag their written partial
   unsigned long long* trace;     // [tile][CG][2] global-timer stamps, or null
   unsigned long long* phases;    // [CTA][8] stamps (see gemm_ws_debug_phases), or null
 #endif
@@ -1022,6 +1023,9 @@ __device__ __forceinline__ void epilogue_role(const Params& p, uint32_t sbase, u
             // scope); the reduction kernel instead runs after this grid.
             bulk_wait<0>();
             fence_proxy_async_global();
+#ifdef GEMM_WS_DEBUG
+            if (p.debug_fault != 2)   // injected fault: the other piece waits in vain
+#endif
             st_release_gpu(sk_written_word(p, C::CS, sk_slot(p, w, w.piece), rank, e), 1u);
 #ifdef GEMM_WS_DEBUG
             if (p.phases && e == 0) p.phases[blockIdx.x * 8 + 6] = global_timer_ns();

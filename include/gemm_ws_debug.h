@@ -26,7 +26,11 @@ extern "C" {
 
 /* Sets the handle's debug state for its later runs.
  *  - fault: 0 none; 1 the stream-out consumer warp returns at once, so the
- *    epilogue's wait for a free slot can only end by the watchdog.
+ *    epilogue's wait for a free slot can only end by the watchdog; 2 split
+ *    pieces that write their partial for the in-kernel fix-up never set
+ *    their written flag, so the piece that adds it can only stop waiting by
+ *    the watchdog (its fix-up words are then left part-way, for
+ *    gemm_ws_query_status to clear).
  *  - trace: device buffer of num_units * ctas_per_cluster * 2 uint64 (see
  *    gemm_ws_debug_launch_shape) or NULL. For work unit u and CTA rank r
  *    in its cluster, trace[(u*ctas_per_cluster + r)*2] = global time (ns) at which
