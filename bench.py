@@ -775,7 +775,7 @@ def main(argv=None):
                     help="seconds of CPU oracle work: the baseline sample, or the whole "
                          "reference arm")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--overhead-reps", type=int, default=100,
+    ap.add_argument("--overhead-reps", type=int, default=300,
                     help="interleaved plain / stream-out launch pairs for the overhead median")
     ap.add_argument("--kernel-only", action="store_true",
                     help="launch only the GEMM of --workload (for profilers); no contract line")
